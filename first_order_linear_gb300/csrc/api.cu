@@ -1,0 +1,407 @@
+// api.cu -- the extern "C" entry points declared in include/rlca.h:
+// argument validation on the host, launch planning, and launches on the
+// caller's stream.  Nothing here allocates memory or synchronises.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <initializer_list>
+
+#include "internal.h"
+#include "rlca.h"
+
+namespace rlca {
+
+namespace {
+
+constexpr int64_t kMaxT = int64_t(1) << 30;
+constexpr int64_t kMaxE = INT32_MAX;
+
+int next_pow2(int64_t x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+std::atomic<int> g_sm_count[256];
+
+cudaError_t sm_count_of_current_device(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 256) {
+    int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return cudaSuccess;
+    }
+  }
+  int c = 0;
+  e = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 256) g_sm_count[dev].store(c, std::memory_order_relaxed);
+  *out = c;
+  return cudaSuccess;
+}
+
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlap(const Span& a, const Span& b) {
+  if (a.p == nullptr || b.p == nullptr || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// every output against every input and every other output
+bool any_overlap(std::initializer_list<Span> ins, std::initializer_list<Span> outs) {
+  for (const Span& o : outs) {
+    for (const Span& i : ins)
+      if (overlap(o, i)) return true;
+    for (const Span& o2 : outs)
+      if (&o2 != &o && overlap(o, o2)) return true;
+  }
+  return false;
+}
+
+bool aligned(const void* p, uintptr_t a) { return p == nullptr || ((uintptr_t)p % a) == 0; }
+
+// sizes: negative / too large -> invalid; returns 1 when the call is decided
+// (invalid, or empty and therefore done)
+int check_sizes(int64_t E, int64_t T, int* status) {
+  if (E < 0 || T < 0 || E > kMaxE || T > kMaxT) {
+    *status = RLCA_ERR_INVALID_ARG;
+    return 1;
+  }
+  if (E == 0 || T == 0) {
+    *status = RLCA_OK;
+    return 1;
+  }
+  return 0;
+}
+
+bool flags_ok(uint32_t flags, uint32_t allowed) { return (flags & ~allowed) == 0u; }
+
+constexpr uint32_t kLayoutFlags = RLCA_TIME_MAJOR | RLCA_MULTIPASS;
+
+template <class Est>
+int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flags, void* ws, size_t ws_bytes,
+           bool vec_ok, cudaStream_t s) {
+  int sm = 0;
+  if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
+  Plan p;
+  if (!make_plan(kind, E, (int)T, A, flags, sm, &p)) return RLCA_ERR_INVALID_ARG;
+  if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes || !aligned(ws, 16))) return RLCA_ERR_INVALID_ARG;
+  Geom g;
+  g.E = E;
+  g.T = (int)T;
+  g.seg_len = p.seg_len;
+  g.nseg = p.nseg;
+  g.mode = kModeFull;
+  g.vec = (!p.time_major && vec_ok && T % 4 == 0) ? 1 : 0;
+  g.ws = ws;
+  return run_scan(est, p, g, s) == cudaSuccess ? RLCA_OK : RLCA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, Plan* out) {
+  const bool retrace = kind == Kind::Retrace;
+  Plan q = {};
+  q.time_major = (flags & RLCA_TIME_MAJOR) != 0;
+  if (q.time_major) {
+    const int cmax = retrace ? kRetraceTmMaxWidth : kTmMaxWidth;
+    int C = (int)std::min<int64_t>(next_pow2((T + 7) / 8), cmax);
+    if (flags & RLCA_MULTIPASS) C = std::max(1, C / 4);
+    q.width = C;
+    q.block = 32 * C;
+    q.rows_per_cta = 32;
+    q.tile = 8 * C;
+    q.smem = (size_t)2 * C * 32 * 8;
+    if (retrace) q.smem += (size_t)C * 64 * num_actions * 4 + (size_t)3 * (q.tile + 1) * 32 * 4;
+  } else {
+    const int wmax = retrace ? kRetraceEmMaxWidth : kEmMaxWidth;
+    int W = (int)std::min<int64_t>(next_pow2(std::max<int64_t>((T + 3) / 4, kEmMinWidth)), wmax);
+    if (flags & RLCA_MULTIPASS) W = std::max(kEmMinWidth, W / 4);
+    q.width = W;
+    q.block = std::max(W, 256);
+    q.rows_per_cta = q.block / W;
+    q.tile = 4 * W;
+    const int nwr = W > 32 ? W / 32 : 1;
+    q.smem = nwr > 1 ? (size_t)2 * nwr * 8 : 0;
+    if (retrace)
+      q.smem += (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
+  }
+  q.ntiles = (int)((T + q.tile - 1) / q.tile);
+  q.row_blocks = (E + q.rows_per_cta - 1) / q.rows_per_cta;
+  int nseg = 1;
+  if (flags & RLCA_MULTIPASS) {
+    nseg = q.ntiles >= 2 ? (q.ntiles + 1) / 2 : 1;
+  } else {
+    // split long rows across CTAs only when the rows alone leave the GPU
+    // mostly idle; the second pass re-reads the inputs
+    const int64_t threads = q.row_blocks * q.block;
+    const int64_t target = (int64_t)sm_count * 1024;
+    if (q.ntiles > 1 && 2 * threads < target)
+      nseg = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
+  }
+  const int seg_tiles = (q.ntiles + nseg - 1) / nseg;
+  q.seg_len = seg_tiles * q.tile;
+  q.nseg = (q.ntiles + seg_tiles - 1) / seg_tiles;
+  q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * 8 : 0;
+  if (q.row_blocks * q.nseg > INT32_MAX) return false;
+  if (q.smem > 227 * 1024) return false;
+  *out = q;
+  return true;
+}
+
+}  // namespace rlca
+
+using namespace rlca;
+
+extern "C" {
+
+const char* rlca_status_string(int status) {
+  switch (status) {
+    case RLCA_OK: return "ok";
+    case RLCA_ERR_INVALID_ARG: return "invalid argument";
+    case RLCA_ERR_UNSUPPORTED: return "unsupported argument";
+    case RLCA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int rlca_version(void) { return 100; }
+
+int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions, uint32_t flags, size_t* bytes) {
+  if (bytes == nullptr) return RLCA_ERR_INVALID_ARG;
+  *bytes = 0;
+  Kind kind;
+  switch (estimator) {
+    case RLCA_EST_GAE: kind = Kind::Gae; break;
+    case RLCA_EST_DISCOUNTED_RETURN: kind = Kind::Disc; break;
+    case RLCA_EST_TD_LAMBDA: kind = Kind::TdLambda; break;
+    case RLCA_EST_VTRACE: kind = Kind::Vtrace; break;
+    case RLCA_EST_RETRACE: kind = Kind::Retrace; break;
+    case RLCA_EST_ELIG_TRACE: kind = Kind::Elig; break;
+    case RLCA_EST_PREFIX_SUM: kind = Kind::PrefixSum; break;
+    case RLCA_EST_AFFINE_SCAN: kind = Kind::Affine; break;
+    default: return RLCA_ERR_INVALID_ARG;
+  }
+  const uint32_t allowed =
+      kLayoutFlags | (kind == Kind::PrefixSum ? (RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START) : 0u);
+  if (!flags_ok(flags, allowed)) return RLCA_ERR_INVALID_ARG;
+  if (kind == Kind::Retrace && num_actions < 1) return RLCA_ERR_INVALID_ARG;
+  if (kind == Kind::Retrace && num_actions > RLCA_MAX_ACTIONS) return RLCA_ERR_UNSUPPORTED;
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  int sm = 0;
+  if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
+  Plan p;
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, &p)) return RLCA_ERR_INVALID_ARG;
+  *bytes = p.ws_bytes;
+  return RLCA_OK;
+}
+
+int rlca_gae(const float* rewards, const float* values, const uint8_t* terminated, const uint8_t* truncated,
+             const float* trunc_value, const float* bootstrap, float* advantages, float* returns, int64_t E,
+             int64_t T, float gamma, float lambda, uint32_t flags, void* workspace, size_t workspace_bytes,
+             rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!rewards || !values || !advantages || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
+                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{advantages, nf}, {returns, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) &&
+                   aligned(returns, 16) && aligned(terminated, 4) && aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  if (truncated) {
+    GaeEst<true> e;
+    e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma; e.gl = gamma * lambda;
+    return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  GaeEst<false> e;
+  e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma; e.gl = gamma * lambda;
+  return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_discounted_return(const float* rewards, const uint8_t* terminated, const uint8_t* truncated,
+                           const float* trunc_value, const float* bootstrap, float* returns, int64_t E, int64_t T,
+                           float gamma, uint32_t flags, void* workspace, size_t workspace_bytes,
+                           rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!rewards || !returns || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{rewards, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
+                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{returns, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(returns, 16) && aligned(terminated, 4) && aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  if (truncated) {
+    DiscEst<true> e;
+    e.b = b; e.r = rewards; e.out = returns; e.gamma = gamma;
+    return launch(Kind::Disc, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  DiscEst<false> e;
+  e.b = b; e.r = rewards; e.out = returns; e.gamma = gamma;
+  return launch(Kind::Disc, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_td_lambda(const float* rewards, const float* values, const uint8_t* terminated, const uint8_t* truncated,
+                   const float* trunc_value, const float* bootstrap, float* returns, int64_t E, int64_t T,
+                   float gamma, float lambda, uint32_t flags, void* workspace, size_t workspace_bytes,
+                   rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!rewards || !values || !returns || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
+                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{returns, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(returns, 16) && aligned(terminated, 4) &&
+                   aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  if (truncated) {
+    TdLambdaEst<true> e;
+    e.b = b; e.r = rewards; e.v = values; e.out = returns; e.gamma = gamma; e.gl = gamma * lambda;
+    e.one_minus_lambda = 1.f - lambda;
+    return launch(Kind::TdLambda, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  TdLambdaEst<false> e;
+  e.b = b; e.r = rewards; e.v = values; e.out = returns; e.gamma = gamma; e.gl = gamma * lambda;
+  e.one_minus_lambda = 1.f - lambda;
+  return launch(Kind::TdLambda, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_vtrace(const float* rewards, const float* values, const float* logp_target, const float* logp_behaviour,
+                const uint8_t* terminated, const uint8_t* truncated, const float* trunc_value,
+                const float* bootstrap, float* vs, float* pg_advantages, int64_t E, int64_t T, float gamma,
+                float rho_bar, float c_bar, float lambda, uint32_t flags, void* workspace, size_t workspace_bytes,
+                rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!rewards || !values || !logp_target || !logp_behaviour || !vs || (truncated && !trunc_value))
+    return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{rewards, nf}, {values, nf}, {logp_target, nf}, {logp_behaviour, nf}, {terminated, nb},
+                   {truncated, nb}, {trunc_value, nf}, {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{vs, nf}, {pg_advantages, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(logp_target, 16) &&
+                   aligned(logp_behaviour, 16) && aligned(vs, 16) && aligned(pg_advantages, 16) &&
+                   aligned(terminated, 4) && aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  if (truncated) {
+    VtraceEst<true> e;
+    e.b = b; e.r = rewards; e.v = values; e.lpt = logp_target; e.lpb = logp_behaviour; e.vs = vs;
+    e.pg = pg_advantages; e.gamma = gamma; e.rho_bar = rho_bar; e.c_bar = c_bar; e.lambda = lambda;
+    return launch(Kind::Vtrace, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  VtraceEst<false> e;
+  e.b = b; e.r = rewards; e.v = values; e.lpt = logp_target; e.lpb = logp_behaviour; e.vs = vs;
+  e.pg = pg_advantages; e.gamma = gamma; e.rho_bar = rho_bar; e.c_bar = c_bar; e.lambda = lambda;
+  return launch(Kind::Vtrace, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_retrace(const float* q, const float* pi, const float* mu_a, const int32_t* actions, const float* rewards,
+                 const uint8_t* terminated, const uint8_t* truncated, const float* trunc_value,
+                 const float* bootstrap, float* q_ret, int64_t E, int64_t T, int32_t num_actions, float gamma,
+                 float lambda, uint32_t flags, void* workspace, size_t workspace_bytes, rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (num_actions < 1) return RLCA_ERR_INVALID_ARG;
+  if (num_actions > RLCA_MAX_ACTIONS) return RLCA_ERR_UNSUPPORTED;
+  if (!q || !pi || !mu_a || !actions || !rewards || !q_ret || (truncated && !trunc_value))
+    return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T), nq = nf * (size_t)num_actions;
+  if (any_overlap({{q, nq}, {pi, nq}, {mu_a, nf}, {actions, nf}, {rewards, nf}, {terminated, nb}, {truncated, nb},
+                   {trunc_value, nf}, {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{q_ret, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(q_ret, 16) && aligned(terminated, 4) && aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  const RetraceStage stg{q, pi, mu_a, actions, num_actions, lambda};
+  if (truncated) {
+    RetraceEst<true> e;
+    e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;
+    return launch(Kind::Retrace, e, E, T, num_actions, flags, workspace, workspace_bytes, vec, stream);
+  }
+  RetraceEst<false> e;
+  e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;
+  return launch(Kind::Retrace, e, E, T, num_actions, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_elig_trace(const float* x, const uint8_t* terminated, const uint8_t* truncated, float* out, int64_t E,
+                    int64_t T, float gamma, float lambda, uint32_t flags, void* workspace, size_t workspace_bytes,
+                    rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!x || !out) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{x, nf}, {terminated, nb}, {truncated, nb}, {workspace, workspace_bytes}}, {{out, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(x, 16) && aligned(out, 16) && aligned(terminated, 4) && aligned(truncated, 4);
+  EligEst e;
+  e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.gl = gamma * lambda;
+  return launch(Kind::Elig, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_episodic_prefix_sum(const void* x, int dtype, const uint8_t* terminated, const uint8_t* truncated,
+                             void* out, int64_t E, int64_t T, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags | RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START)) return RLCA_ERR_INVALID_ARG;
+  if (dtype != RLCA_F32 && dtype != RLCA_I32) return RLCA_ERR_INVALID_ARG;
+  if (!x || !out) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{x, nf}, {terminated, nb}, {truncated, nb}, {workspace, workspace_bytes}}, {{out, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(x, 16) && aligned(out, 16) && aligned(terminated, 4) && aligned(truncated, 4);
+  const uint32_t core = flags & kLayoutFlags;
+  const int excl = (flags & RLCA_PSUM_EXCLUSIVE) ? 1 : 0;
+  const int start = (flags & RLCA_PSUM_FLAG_IS_START) ? 1 : 0;
+  if (dtype == RLCA_I32) {
+    PrefixSumEst<uint32_t> e;
+    e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.exclusive = excl; e.flag_is_start = start;
+    return launch(Kind::PrefixSum, e, E, T, 0, core, workspace, workspace_bytes, vec, stream);
+  }
+  PrefixSumEst<float> e;
+  e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.exclusive = excl; e.flag_is_start = start;
+  return launch(Kind::PrefixSum, e, E, T, 0, core, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_affine_scan(const float* alpha, const float* beta, const float* carry, float* out, int64_t E, int64_t T,
+                     int reverse, uint32_t flags, void* workspace, size_t workspace_bytes, rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!alpha || !beta || !out) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4;
+  if (any_overlap({{alpha, nf}, {beta, nf}, {carry, (size_t)E * 4}, {workspace, workspace_bytes}}, {{out, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(alpha, 16) && aligned(beta, 16) && aligned(out, 16);
+  if (reverse) {
+    AffineEst<true> e;
+    e.alpha = alpha; e.beta = beta; e.carry = carry; e.out = out;
+    return launch(Kind::Affine, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  AffineEst<false> e;
+  e.alpha = alpha; e.beta = beta; e.carry = carry; e.out = out;
+  return launch(Kind::Affine, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// dispatch.cuh -- kernel selection by plan width and launch on the caller's stream.
+#pragma once
+
+#include "internal.h"
+
+namespace rlca {
+
+template <class Est>
+struct WidthCaps {
+  static constexpr int em = kEmMaxWidth;
+  static constexpr int tm = kTmMaxWidth;
+};
+template <bool H>
+struct WidthCaps<RetraceEst<H>> {
+  static constexpr int em = kRetraceEmMaxWidth;
+  static constexpr int tm = kRetraceTmMaxWidth;
+};
+
+template <class Est>
+static cudaError_t launch_one(void (*kernel)(Est, Geom), const Plan& p, const Est& est, const Geom& g,
+                              cudaStream_t s) {
+  if (p.smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.row_blocks * p.nseg));
+  cfg.blockDim = dim3((unsigned)p.block);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, kernel, est, g);
+}
+
+template <class Est, int W>
+static cudaError_t launch_em_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (W <= WidthCaps<Est>::em) {
+    return launch_one<Est>(em_scan_kernel<Est, W>, p, est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est, int C>
+static cudaError_t launch_tm_c(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (C <= WidthCaps<Est>::tm) {
+    return launch_one<Est>(tm_scan_kernel<Est, C>, p, est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est>
+static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if (p.time_major) {
+    switch (p.width) {
+      case 1: return launch_tm_c<Est, 1>(p, est, g, s);
+      case 2: return launch_tm_c<Est, 2>(p, est, g, s);
+      case 4: return launch_tm_c<Est, 4>(p, est, g, s);
+      case 8: return launch_tm_c<Est, 8>(p, est, g, s);
+      case 16: return launch_tm_c<Est, 16>(p, est, g, s);
+      case 32: return launch_tm_c<Est, 32>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  switch (p.width) {
+    case 4: return launch_em_w<Est, 4>(p, est, g, s);
+    case 8: return launch_em_w<Est, 8>(p, est, g, s);
+    case 16: return launch_em_w<Est, 16>(p, est, g, s);
+    case 32: return launch_em_w<Est, 32>(p, est, g, s);
+    case 64: return launch_em_w<Est, 64>(p, est, g, s);
+    case 128: return launch_em_w<Est, 128>(p, est, g, s);
+    case 256: return launch_em_w<Est, 256>(p, est, g, s);
+    case 512: return launch_em_w<Est, 512>(p, est, g, s);
+    case 1024: return launch_em_w<Est, 1024>(p, est, g, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est>
+cudaError_t run_scan(const Est& est, const Plan& p, const Geom& g0, cudaStream_t s) {
+  Geom g = g0;
+  if (p.nseg > 1) {
+    g.mode = kModeAggregate;
+    cudaError_t e = launch_pass(p, est, g, s);
+    if (e != cudaSuccess) return e;
+  }
+  g.mode = kModeFull;
+  return launch_pass(p, est, g, s);
+}
+
+}  // namespace rlca

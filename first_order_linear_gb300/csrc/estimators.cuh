@@ -1,0 +1,671 @@
+// estimators.cuh -- per-estimator coefficient construction for the scan drivers.
+//
+// Each functor turns raw rollout inputs into the (alpha_t, beta_t) of the
+// recurrence in registers, as rl-triton (arXiv:2608.17641) §3.1 describes
+// (fused kernels build the coefficients on chip from the raw rollout
+// tensors), with the episode-boundary rules of §3.2:
+//   termination  -> successor value 0, beta_t = 0
+//   truncation   -> successor value trunc_value[t], beta_t = 0
+//                   (termination wins where both flags are set)
+//   t = T-1      -> successor value bootstrap, either inside alpha_{T-1}
+//                   (GAE, V-Trace, Retrace; beta_{T-1} = 0) or through the
+//                   scan carry A_T = bootstrap (TD(lambda), discounted return)
+//   forward scans restart after a flagged step (§5: beta_t = 0 when d_{t-1} = 1).
+//
+// Interface used by the drivers of scan_core.cuh:
+//   V, kBackward, kNb           value type, scan direction, neighbour floats
+//   Regs<L>                     per-thread registers of L consecutive steps
+//   row_carry(row)              A_T (backward) / A_{-1} (forward) of a row
+//   stage / stage_tm            cooperative per-tile staging (Retrace only)
+//   load(...)                   read the thread's L steps
+//   nb_give / nb_load / nb_take the neighbour step's inputs (step t0+L for a
+//                               backward scan, t0-1 for a forward one)
+//   coef(R, k, t)               (alpha_t, beta_t) of step t = t0 + k
+//   emit(R, k, A, adj, c)       output of step k from A_t (adj = A of the
+//                               step the recurrence reads)
+//   store(...)                  write the thread's outputs
+#pragma once
+
+#include <type_traits>
+
+#include "scan_core.cuh"
+
+namespace rlca {
+
+// Default no-op staging.
+struct NoStage {
+  template <int ROWS, int BLOCK, class Lay>
+  __device__ __forceinline__ void stage(const Lay&, int64_t, int, int, int, unsigned char*) const {}
+  template <int BLOCK, class Lay>
+  __device__ __forceinline__ void stage_tm(const Lay&, int64_t, int, int, unsigned char*) const {}
+};
+
+// Common boundary inputs of the backward estimators.
+struct BoundaryArgs {
+  const uint8_t* term;   // nullable
+  const uint8_t* trunc;  // nullable (HAS_TRUNC == false ignores it)
+  const float* tv;       // read where trunc is set
+  const float* boot;     // [E], nullable
+  int T;
+};
+
+template <int L>
+struct BoundaryRegs {
+  uint32_t term, trunc;  // bit k: flag of step t0+k (trunc already cleared where term is set)
+  float tv[L];
+  float boot;            // bootstrap of the row when this thread holds step T-1
+};
+
+template <bool HAS_TRUNC, int L, class Lay>
+__device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryRegs<L>& R, const Lay& lay,
+                                              int64_t row, int t0, int n, bool vec) {
+  R.term = load_flags<L>(b.term, lay, row, t0, n, vec);
+  R.trunc = HAS_TRUNC ? (load_flags<L>(b.trunc, lay, row, t0, n, vec) & ~R.term) : 0u;
+#pragma unroll
+  for (int k = 0; k < L; ++k)
+    R.tv[k] = (HAS_TRUNC && ((R.trunc >> k) & 1u)) ? __ldg(b.tv + lay.at(row, t0 + k)) : 0.f;
+  R.boot = (n > 0 && t0 + n == b.T && b.boot != nullptr) ? __ldg(b.boot + row) : 0.f;
+}
+
+// successor value of step k: 0 / trunc value / bootstrap / interior value
+template <int L>
+__device__ __forceinline__ float successor(const BoundaryRegs<L>& R, int k, int t, int T, float interior) {
+  float s = (t == T - 1) ? R.boot : interior;
+  if ((R.trunc >> k) & 1u) s = R.tv[k];
+  if ((R.term >> k) & 1u) s = 0.f;
+  return s;
+}
+
+template <int L>
+__device__ __forceinline__ bool cut(const BoundaryRegs<L>& R, int k) {
+  return ((R.term | R.trunc) >> k) & 1u;
+}
+
+// ===========================================================================
+// GAE (rl-triton §2.1; Schulman et al. 2016)
+//   alpha_t = delta_t = r_t + gamma V_next(t) - V_t
+//   beta_t  = gamma lambda (1 - d_t) [t < T-1],    carry 0
+//   outputs adv_t = A_t, ret_t = A_t + V_t
+// ===========================================================================
+template <bool HAS_TRUNC>
+struct GaeEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 1;
+  BoundaryArgs b;
+  const float* r;
+  const float* v;
+  float* adv;
+  float* ret;  // nullable
+  float gamma, gl;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], v[L], vnext;
+    float oa[L], orr[L];
+  };
+  __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_vals<L>(v, lay, row, t0, n, vec, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+    R.vnext = 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = __ldg(v + lay.at(row, t));
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const float vn = successor(R.bd, k, t, b.T, (k + 1 < L) ? R.v[k + 1] : R.vnext);
+    const float delta = R.r[k] + gamma * vn - R.v[k];
+    const float beta = (cut(R.bd, k) || t == b.T - 1) ? 0.f : gl;
+    return {delta, beta};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.oa[k] = A;
+    R.orr[k] = A + R.v[k];
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(adv, lay, row, t0, n, vec, R.oa);
+    if (ret != nullptr) store_vals<L>(ret, lay, row, t0, n, vec, R.orr);
+  }
+};
+
+// ===========================================================================
+// Discounted return
+//   alpha_t = r_t + gamma trunc_t trunc_value_t,  beta_t = gamma (1 - d_t),
+//   carry A_T = bootstrap
+// ===========================================================================
+template <bool HAS_TRUNC>
+struct DiscEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 0;
+  BoundaryArgs b;
+  const float* r;
+  float* out;
+  float gamma;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], o[L];
+  };
+  __device__ __forceinline__ float row_carry(int64_t row) const {
+    return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay&, int64_t, int, float*) const {}
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>&, const float*) const {}
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int) const {
+    const bool tr = (R.bd.trunc >> k) & 1u;
+    const float alpha = tr ? R.r[k] + gamma * R.bd.tv[k] : R.r[k];
+    return {alpha, cut(R.bd, k) ? 0.f : gamma};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+// ===========================================================================
+// TD(lambda) return
+//   alpha_t = r_t + gamma [trunc_t tv_t + (1 - d_t)(1 - lambda) V_next(t)]
+//   beta_t  = gamma lambda (1 - d_t),   carry A_T = bootstrap
+// ===========================================================================
+template <bool HAS_TRUNC>
+struct TdLambdaEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 1;
+  BoundaryArgs b;
+  const float* r;
+  const float* v;
+  float* out;
+  float gamma, gl, one_minus_lambda;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], v[L], vnext, o[L];
+  };
+  __device__ __forceinline__ float row_carry(int64_t row) const {
+    return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_vals<L>(v, lay, row, t0, n, vec, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+    R.vnext = 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = __ldg(v + lay.at(row, t));
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const bool tm = (R.bd.term >> k) & 1u, tr = (R.bd.trunc >> k) & 1u;
+    const float vn = (t == b.T - 1) ? R.bd.boot : ((k + 1 < L) ? R.v[k + 1] : R.vnext);
+    const float tail = tm ? 0.f : (tr ? R.bd.tv[k] : one_minus_lambda * vn);
+    return {R.r[k] + gamma * tail, (tm || tr) ? 0.f : gl};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+// ===========================================================================
+// V-Trace (rl-triton §8; Espeholt et al. 2018)
+//   rho_t = min(rho_bar, ratio_t),  c_t = lambda min(c_bar, ratio_t)
+//   alpha_t = rho_t (r_t + gamma V_next(t) - V_t)
+//   beta_t  = gamma c_t (1 - d_t) [t < T-1],   carry 0
+//   vs_t = V_t + A_t;  pg_t = rho_t (r_t + gamma vs_next(t) - V_t)
+// ===========================================================================
+template <bool HAS_TRUNC>
+struct VtraceEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 1;
+  BoundaryArgs b;
+  const float* r;
+  const float* v;
+  const float* lpt;
+  const float* lpb;
+  float* vs;
+  float* pg;  // nullable
+  float gamma, rho_bar, c_bar, lambda;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], v[L], rho[L], c[L], vnext;
+    float ovs[L], opg[L];
+    int t0;
+  };
+  __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    float a[L], bb[L];
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_vals<L>(v, lay, row, t0, n, vec, R.v);
+    load_vals<L>(lpt, lay, row, t0, n, vec, a);
+    load_vals<L>(lpb, lay, row, t0, n, vec, bb);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const float ratio = expf(a[k] - bb[k]);
+      R.rho[k] = fminf(rho_bar, ratio);
+      R.c[k] = lambda * fminf(c_bar, ratio);
+    }
+    R.vnext = 0.f;
+    R.t0 = t0;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = __ldg(v + lay.at(row, t));
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const float vn = successor(R.bd, k, t, b.T, (k + 1 < L) ? R.v[k + 1] : R.vnext);
+    const float delta = R.rho[k] * (R.r[k] + gamma * vn - R.v[k]);
+    const float beta = (cut(R.bd, k) || t == b.T - 1) ? 0.f : gamma * R.c[k];
+    return {delta, beta};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float adj, const Aff<float>&) const {
+    R.ovs[k] = R.v[k] + A;
+    const float vn = (k + 1 < L) ? R.v[k + 1] : R.vnext;
+    const float nvs = successor(R.bd, k, R.t0 + k, b.T, vn + adj);
+    R.opg[k] = R.rho[k] * (R.r[k] + gamma * nvs - R.v[k]);
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(vs, lay, row, t0, n, vec, R.ovs);
+    if (pg != nullptr) store_vals<L>(pg, lay, row, t0, n, vec, R.opg);
+  }
+};
+
+// ===========================================================================
+// Retrace(lambda) (rl-triton §3.3; Munos et al. 2016)
+//   per step (reduced over the action axis on chip, before the scan):
+//     EV_t = sum_a pi[t,a] Q[t,a],  Qa_t = Q[t,a_t],  c_t = lambda min(1, pi[t,a_t] / mu_a[t])
+//   alpha_t = r_t + gamma (EV_{t+1} - c_{t+1} Qa_{t+1})   inside an episode
+//           = r_t (termination) / r_t + gamma tv_t (truncation) / r_t + gamma bootstrap (t = T-1)
+//   beta_t  = gamma c_{t+1} (1 - d_t) [t < T-1],   carry 0
+// The per-step reduction stages the [items, A] blocks of Q and pi through
+// shared memory with coalesced loads; each tile stages its steps plus the
+// first step after it (the last step's successor).
+// ===========================================================================
+struct RetraceStage {
+  const float* q;
+  const float* pi;
+  const float* mu_a;
+  const int32_t* act;
+  int A;
+  float lambda;
+
+  // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous);
+  // item s writes its three scalars at index `slot` of the dst arrays
+  __device__ __forceinline__ void chunk(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p, float* dst_ev,
+                                        float* dst_qa, float* dst_c, int slot) const {
+    const float* qb = q + e0 * A;
+    const float* pb = pi + e0 * A;
+    const int total = cnt * A;
+#pragma unroll 6
+    for (int f = lane; f < total; f += 32) {
+      raw_q[f] = __ldg(qb + f);
+      raw_p[f] = __ldg(pb + f);
+    }
+    __syncwarp();
+    if (lane < cnt) {
+      const float* rq = raw_q + lane * A;
+      const float* rp = raw_p + lane * A;
+      float ev = 0.f;
+      for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
+      int at = __ldg(act + e0 + lane);
+      at = at < 0 ? 0 : (at >= A ? A - 1 : at);
+      const float pa = rp[at];
+      const float mu = __ldg(mu_a + e0 + lane);
+      dst_ev[slot] = ev;
+      dst_qa[slot] = rq[at];
+      dst_c[slot] = lambda * fminf(1.f, pa / mu);
+    }
+    __syncwarp();
+  }
+};
+
+template <bool HAS_TRUNC>
+struct RetraceEst {
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 0;
+  BoundaryArgs b;
+  RetraceStage st;
+  const float* r;
+  float* out;
+  float gamma;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], evn[L], qan[L], cn[L], o[L];
+  };
+  __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
+
+  // shared memory: per warp raw Q and pi blocks [32 * A] each, then the
+  // staged per-step scalars [3][ROWS][tile + 1]
+  template <int ROWS, int BLOCK, class Lay>
+  __device__ __forceinline__ void stage(const Lay& lay, int64_t row0, int, int ts, int te,
+                                        unsigned char* sm) const {
+    constexpr int NW = BLOCK / 32;
+    constexpr int SROW = 4 * (BLOCK / ROWS) + 1;  // tile + 1 steps per row
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* raw_q = reinterpret_cast<float*>(sm) + warp * 64 * st.A;
+    float* raw_p = raw_q + 32 * st.A;
+    float* s_ev = reinterpret_cast<float*>(sm) + NW * 64 * st.A;
+    float* s_qa = s_ev + ROWS * SROW;
+    float* s_c = s_qa + ROWS * SROW;
+    const int nst = te - ts + (te < b.T ? 1 : 0);
+    const int per_row = (nst + 31) / 32;
+    for (int ch = warp; ch < ROWS * per_row; ch += NW) {
+      const int rr = ch / per_row, m = ch - rr * per_row;
+      if (row0 + rr >= lay.E) continue;
+      const int i0 = m * 32;
+      st.chunk(lay.at(row0 + rr, ts + i0), min(32, nst - i0), lane, raw_q, raw_p, s_ev, s_qa, s_c,
+               rr * SROW + i0 + lane);
+    }
+    __syncthreads();
+  }
+  // time-major: one chunk = one step of 32 consecutive environments;
+  // staged scalars [3][tile + 1][32]
+  template <int BLOCK, class Lay>
+  __device__ __forceinline__ void stage_tm(const Lay& lay, int64_t row0, int ts, int te, unsigned char* sm) const {
+    constexpr int NW = BLOCK / 32;
+    constexpr int SROWS = (BLOCK / 32) * 8 + 1;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* raw_q = reinterpret_cast<float*>(sm) + warp * 64 * st.A;
+    float* raw_p = raw_q + 32 * st.A;
+    float* s_ev = reinterpret_cast<float*>(sm) + NW * 64 * st.A;
+    float* s_qa = s_ev + SROWS * 32;
+    float* s_c = s_qa + SROWS * 32;
+    const int nst = te - ts + (te < b.T ? 1 : 0);
+    const int cnt = (int)min((int64_t)32, lay.E - row0);
+    for (int i = warp; i < nst; i += NW)
+      st.chunk(lay.at(row0, ts + i), cnt, lane, raw_q, raw_p, s_ev, s_qa, s_c, i * 32 + lane);
+    __syncthreads();
+  }
+
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int slot, int t0, int n,
+                                       bool vec, int ts, int tile, unsigned char* sm) const {
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+    constexpr bool kTM = Lay::kTimeMajor;
+    const int NW = blockDim.x >> 5;
+    const float* s_ev = reinterpret_cast<const float*>(sm) + NW * 64 * st.A;
+    const int srows = tile + 1;
+    const int plane = kTM ? srows * 32 : srows * (int)(blockDim.x / (tile / 4));
+    const float* s_qa = s_ev + plane;
+    const float* s_c = s_qa + plane;
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const int t = t0 + k + 1;  // successor step
+      if (k < n && t < b.T) {
+        const int i = t - ts;
+        const int idx = kTM ? i * 32 + slot : slot * srows + i;
+        R.evn[k] = s_ev[idx];
+        R.qan[k] = s_qa[idx];
+        R.cn[k] = s_c[idx];
+      } else {
+        R.evn[k] = 0.f;
+        R.qan[k] = 0.f;
+        R.cn[k] = 0.f;
+      }
+    }
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay&, int64_t, int, float*) const {}
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>&, const float*) const {}
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const bool tm = (R.bd.term >> k) & 1u, tr = (R.bd.trunc >> k) & 1u;
+    const bool last = t == b.T - 1;
+    const float interior = R.evn[k] - R.cn[k] * R.qan[k];
+    const float tail = tm ? 0.f : (tr ? R.bd.tv[k] : (last ? R.bd.boot : interior));
+    const float beta = (tm || tr || last) ? 0.f : gamma * R.cn[k];
+    return {R.r[k] + gamma * tail, beta};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+// ===========================================================================
+// Eligibility trace, forward (rl-triton §1, §5)
+//   alpha_t = x_t,  beta_t = gamma lambda (1 - d_{t-1}),  e_{-1} = 0
+// ===========================================================================
+struct EligEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = false;
+  static constexpr int kNb = 1;
+  const float* x;
+  const uint8_t* term;   // nullable
+  const uint8_t* trunc;  // nullable
+  float* out;
+  float gl;
+
+  template <int L>
+  struct Regs {
+    float x[L], o[L];
+    uint32_t done;
+    float prev_done;
+  };
+  __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    load_vals<L>(x, lay, row, t0, n, vec, R.x);
+    R.done = load_flags<L>(term, lay, row, t0, n, vec) | load_flags<L>(trunc, lay, row, t0, n, vec);
+    R.prev_done = 1.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const {
+    g[0] = ((R.done >> (L - 1)) & 1u) ? 1.f : 0.f;
+  }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = (load_flag1(term, lay, row, t) || load_flag1(trunc, lay, row, t)) ? 1.f : 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.prev_done = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const bool start = (t == 0) || (k == 0 ? R.prev_done != 0.f : ((R.done >> (k - 1)) & 1u) != 0u);
+    return {R.x[k], start ? 0.f : gl};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+// ===========================================================================
+// Episodic prefix sum, segmented forward scan (rl-triton §3.3)
+//   alpha_t = x_t,  beta_t = 1 - start_t, where start_t = d_{t-1} (flag ends
+//   an episode) or d_t (flag starts one), and start_0 = 1.
+//   exclusive output: beta_t * A_{t-1}.
+// int32 runs in uint32 arithmetic (wraps modulo 2^32; beta is 0 or 1, so any
+// grouping gives the same bits).
+// ===========================================================================
+template <class VT>
+struct PrefixSumEst : NoStage {
+  using V = VT;
+  static constexpr bool kBackward = false;
+  static constexpr int kNb = 1;
+  const void* x;
+  const uint8_t* term;
+  const uint8_t* trunc;
+  void* out;
+  int exclusive;
+  int flag_is_start;
+
+  template <int L>
+  struct Regs {
+    V x[L], o[L];
+    uint32_t done;
+    float prev_done;
+  };
+  __device__ __forceinline__ V row_carry(int64_t) const { return V(0); }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    if constexpr (std::is_integral<V>::value) {
+      load_ints<L>(static_cast<const int32_t*>(x), lay, row, t0, n, vec, R.x);
+    } else {
+      load_vals<L>(static_cast<const float*>(x), lay, row, t0, n, vec, R.x);
+    }
+    R.done = load_flags<L>(term, lay, row, t0, n, vec) | load_flags<L>(trunc, lay, row, t0, n, vec);
+    R.prev_done = 1.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const {
+    g[0] = ((R.done >> (L - 1)) & 1u) ? 1.f : 0.f;
+  }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = (load_flag1(term, lay, row, t) || load_flag1(trunc, lay, row, t)) ? 1.f : 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.prev_done = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<V> coef(const Regs<L>& R, int k, int t) const {
+    bool start;
+    if (flag_is_start)
+      start = (t == 0) || ((R.done >> k) & 1u);
+    else
+      start = (t == 0) || (k == 0 ? R.prev_done != 0.f : ((R.done >> (k - 1)) & 1u) != 0u);
+    return {R.x[k], start ? V(0) : V(1)};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, V A, V adj, const Aff<V>& c) const {
+    R.o[k] = exclusive ? (c.b != V(0) ? adj : V(0)) : A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    if constexpr (std::is_integral<V>::value) {
+      store_ints<L>(static_cast<int32_t*>(out), lay, row, t0, n, vec, R.o);
+    } else {
+      store_vals<L>(static_cast<float*>(out), lay, row, t0, n, vec, R.o);
+    }
+  }
+};
+
+// ===========================================================================
+// Generic affine scan over precomputed coefficients (rl-triton §4)
+// ===========================================================================
+template <bool BWD>
+struct AffineEst : NoStage {
+  using V = float;
+  static constexpr bool kBackward = BWD;
+  static constexpr int kNb = 0;
+  const float* alpha;
+  const float* beta;
+  const float* carry;  // [E], nullable
+  float* out;
+
+  template <int L>
+  struct Regs {
+    float a[L], b[L], o[L];
+  };
+  __device__ __forceinline__ float row_carry(int64_t row) const {
+    return carry != nullptr ? __ldg(carry + row) : 0.f;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, unsigned char*) const {
+    load_vals<L>(alpha, lay, row, t0, n, vec, R.a);
+    load_vals<L>(beta, lay, row, t0, n, vec, R.b);
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay&, int64_t, int, float*) const {}
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>&, const float*) const {}
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int) const {
+    return {R.a[k], R.b[k]};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+}  // namespace rlca

@@ -1,0 +1,46 @@
+// internal.h -- host-side launch planning shared by the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "estimators.cuh"
+
+namespace rlca {
+
+enum class Kind { Gae, Disc, TdLambda, Vtrace, Retrace, Elig, PrefixSum, Affine };
+
+// Largest env-major threads-per-row and time-major chunk-threads per
+// environment of a kind (Retrace keeps its tiles small: it stages its
+// per-action blocks in shared memory).
+constexpr int kEmMaxWidth = 1024;
+constexpr int kTmMaxWidth = 32;
+constexpr int kRetraceEmMaxWidth = 256;
+constexpr int kRetraceTmMaxWidth = 8;
+constexpr int kEmMinWidth = 4;
+
+struct Plan {
+  bool time_major;
+  int width;        // env-major: threads per row; time-major: chunk-threads per environment
+  int block;        // threads per CTA
+  int rows_per_cta;
+  int tile;         // steps per tile
+  int ntiles;       // tiles per row
+  int nseg;         // segments per row (> 1: two-pass)
+  int seg_len;      // steps per segment
+  int64_t row_blocks;
+  size_t smem;      // dynamic shared memory per CTA
+  size_t ws_bytes;  // workspace of the two-pass path
+};
+
+// Fills *p for a problem; returns false when the sizes cannot be launched.
+bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, Plan* p);
+
+// Launches the scan of one estimator functor (both passes of the two-pass
+// path when p.nseg > 1).  Defined by explicit instantiation in the family
+// translation units.
+template <class Est>
+cudaError_t run_scan(const Est& est, const Plan& p, const Geom& g, cudaStream_t s);
+
+}  // namespace rlca

@@ -1,0 +1,12 @@
+// Kernels of the value-target estimators: GAE, discounted return, TD(lambda).
+#include "dispatch.cuh"
+
+namespace rlca {
+template cudaError_t run_scan<GaeEst<true>>(const GaeEst<true>&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<GaeEst<false>>(const GaeEst<false>&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<DiscEst<true>>(const DiscEst<true>&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<DiscEst<false>>(const DiscEst<false>&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<TdLambdaEst<true>>(const TdLambdaEst<true>&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<TdLambdaEst<false>>(const TdLambdaEst<false>&, const Plan&, const Geom&,
+                                                  cudaStream_t);
+}  // namespace rlca
