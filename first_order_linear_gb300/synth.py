@@ -2,9 +2,9 @@
 
 This module only draws inputs: it holds none of the estimators' arithmetic,
 so the CUDA path and the float64 oracle can both be fed from it without
-sharing any computation.  Every draw comes from one CPU
-``torch.Generator`` seeded per workload, in a fixed order, so a seed fixes
-the inputs bit for bit on any machine with the same PyTorch CPU generator.
+sharing any computation.  Every draw comes from one ``torch.Generator``
+(on the device the arrays are made on) seeded per workload, in a fixed
+order, so a seed and a device type fix the inputs bit for bit.
 
 The workloads follow the shapes and distributions of the rl-triton paper
 (arXiv:2608.17641) benchmarks, "massively parallel simulation regime"
@@ -15,8 +15,10 @@ value for the rollout-window edge, and a dense truncation-value tensor that
 is only read where a step is truncated.  The policy inputs of V-Trace and
 Retrace(lambda) come from 18-action softmax / log-softmax of N(0, 1) logits.
 
-All arrays are numpy, env-major ``[E, T]`` (``[E, T, A]`` for per-action
-tensors); :func:`to_time_major` re-lays them out as ``[T, E]``.
+Arrays are torch tensors on the requested device (CPU by default),
+env-major ``[E, T]`` (``[E, T, A]`` for per-action tensors);
+:func:`to_time_major` re-lays them out as ``[T, E]`` and :func:`numpy`
+turns a dict of them into numpy arrays.
 """
 from __future__ import annotations
 
@@ -28,8 +30,8 @@ import torch
 NUM_ACTIONS = 18
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator()
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
 
@@ -37,9 +39,15 @@ def _gen(seed: int) -> torch.Generator:
 def _flags(g: torch.Generator, E: int, T: int, p_term: float, p_trunc: float):
     """Termination then truncation flags as uint8, truncation cleared where
     the step also terminates (the two are drawn disjoint)."""
-    term = torch.rand(E, T, generator=g) < p_term
-    trunc = (torch.rand(E, T, generator=g) < p_trunc) & ~term
-    return term.to(torch.uint8).numpy(), trunc.to(torch.uint8).numpy()
+    dev = g.device
+    term = torch.rand(E, T, generator=g, device=dev) < p_term
+    trunc = (torch.rand(E, T, generator=g, device=dev) < p_trunc) & ~term
+    return term.to(torch.uint8), trunc.to(torch.uint8)
+
+
+def numpy(d: dict) -> dict:
+    """The same dict with every tensor as a CPU numpy array."""
+    return {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
 def config_seed(name: str) -> int:
@@ -47,8 +55,8 @@ def config_seed(name: str) -> int:
     return zlib.crc32(name.encode()) & 0x7FFFFFFF
 
 
-def value_rollout(E: int, T: int, seed: int, p_term: float = 0.05,
-                  p_trunc: float = 0.02, with_trunc: bool = True) -> dict:
+def value_rollout(E: int, T: int, seed: int, p_term: float = 0.05, p_trunc: float = 0.02,
+                  with_trunc: bool = True, device="cpu") -> dict:
     """Inputs of GAE, TD(lambda) and discounted returns.
 
     Draw order: rewards [E,T], values [E,T], bootstrap [E], trunc_value
@@ -56,20 +64,19 @@ def value_rollout(E: int, T: int, seed: int, p_term: float = 0.05,
     the truncation flags are still drawn (so the other arrays do not move)
     but returned as ``None``.
     """
-    g = _gen(seed)
-    rewards = torch.randn(E, T, generator=g).numpy()
-    values = torch.randn(E, T, generator=g).numpy()
-    bootstrap = torch.randn(E, generator=g).numpy()
-    trunc_value = torch.randn(E, T, generator=g).numpy()
+    g = _gen(seed, device)
+    rewards = torch.randn(E, T, generator=g, device=device)
+    values = torch.randn(E, T, generator=g, device=device)
+    bootstrap = torch.randn(E, generator=g, device=device)
+    trunc_value = torch.randn(E, T, generator=g, device=device)
     term, trunc = _flags(g, E, T, p_term, p_trunc)
     return dict(rewards=rewards, values=values, bootstrap=bootstrap,
                 trunc_value=trunc_value if with_trunc else None,
                 terminated=term, truncated=trunc if with_trunc else None)
 
 
-def vtrace_rollout(E: int, T: int, seed: int, p_term: float = 0.01,
-                   p_trunc: float = 0.0, with_trunc: bool = False,
-                   num_actions: int = NUM_ACTIONS) -> dict:
+def vtrace_rollout(E: int, T: int, seed: int, p_term: float = 0.01, p_trunc: float = 0.0,
+                   with_trunc: bool = False, num_actions: int = NUM_ACTIONS, device="cpu") -> dict:
     """Inputs of V-Trace.
 
     Target and behaviour logits are N(0,1) over ``num_actions``; the taken
@@ -78,13 +85,13 @@ def vtrace_rollout(E: int, T: int, seed: int, p_term: float = 0.01,
     Draw order: rewards, values, bootstrap, trunc_value, target logits,
     behaviour logits, sampled actions, flags.
     """
-    g = _gen(seed)
-    rewards = torch.randn(E, T, generator=g)
-    values = torch.randn(E, T, generator=g)
-    bootstrap = torch.randn(E, generator=g)
-    trunc_value = torch.randn(E, T, generator=g)
-    logits_pi = torch.randn(E, T, num_actions, generator=g)
-    logits_mu = torch.randn(E, T, num_actions, generator=g)
+    g = _gen(seed, device)
+    rewards = torch.randn(E, T, generator=g, device=device)
+    values = torch.randn(E, T, generator=g, device=device)
+    bootstrap = torch.randn(E, generator=g, device=device)
+    trunc_value = torch.randn(E, T, generator=g, device=device)
+    logits_pi = torch.randn(E, T, num_actions, generator=g, device=device)
+    logits_mu = torch.randn(E, T, num_actions, generator=g, device=device)
     logp_pi = torch.log_softmax(logits_pi, dim=-1)
     logp_mu = torch.log_softmax(logits_mu, dim=-1)
     # the taken action is sampled from the behaviour policy
@@ -93,18 +100,15 @@ def vtrace_rollout(E: int, T: int, seed: int, p_term: float = 0.01,
     lp_pi = torch.gather(logp_pi, -1, actions).squeeze(-1)
     lp_mu = torch.gather(logp_mu, -1, actions).squeeze(-1)
     term, trunc = _flags(g, E, T, p_term, p_trunc)
-    return dict(rewards=rewards.numpy(), values=values.numpy(),
-                bootstrap=bootstrap.numpy(),
-                trunc_value=trunc_value.numpy() if with_trunc else None,
-                logp_target=lp_pi.contiguous().numpy(),
-                logp_behaviour=lp_mu.contiguous().numpy(),
-                actions=actions.squeeze(-1).to(torch.int32).numpy(),
+    return dict(rewards=rewards, values=values, bootstrap=bootstrap,
+                trunc_value=trunc_value if with_trunc else None,
+                logp_target=lp_pi.contiguous(), logp_behaviour=lp_mu.contiguous(),
+                actions=actions.squeeze(-1).to(torch.int32),
                 terminated=term, truncated=trunc if with_trunc else None)
 
 
-def retrace_rollout(E: int, T: int, seed: int, p_term: float = 0.002,
-                    p_trunc: float = 0.0, with_trunc: bool = False,
-                    num_actions: int = NUM_ACTIONS) -> dict:
+def retrace_rollout(E: int, T: int, seed: int, p_term: float = 0.002, p_trunc: float = 0.0,
+                    with_trunc: bool = False, num_actions: int = NUM_ACTIONS, device="cpu") -> dict:
     """Inputs of Retrace(lambda).
 
     Q [E,T,A] ~ N(0,1); target policy pi = softmax(N(0,1) logits) [E,T,A];
@@ -114,58 +118,57 @@ def retrace_rollout(E: int, T: int, seed: int, p_term: float = 0.002,
     Draw order: rewards, Q, target logits, behaviour logits, actions,
     bootstrap, trunc_value, flags.
     """
-    g = _gen(seed)
-    rewards = torch.randn(E, T, generator=g)
-    q = torch.randn(E, T, num_actions, generator=g)
-    pi = torch.softmax(torch.randn(E, T, num_actions, generator=g), dim=-1)
-    mu = torch.softmax(torch.randn(E, T, num_actions, generator=g), dim=-1)
-    actions = torch.randint(0, num_actions, (E, T), generator=g)
-    bootstrap = torch.randn(E, generator=g)
-    trunc_value = torch.randn(E, T, generator=g)
+    g = _gen(seed, device)
+    rewards = torch.randn(E, T, generator=g, device=device)
+    q = torch.randn(E, T, num_actions, generator=g, device=device)
+    pi = torch.softmax(torch.randn(E, T, num_actions, generator=g, device=device), dim=-1)
+    mu = torch.softmax(torch.randn(E, T, num_actions, generator=g, device=device), dim=-1)
+    actions = torch.randint(0, num_actions, (E, T), generator=g, device=device)
+    bootstrap = torch.randn(E, generator=g, device=device)
+    trunc_value = torch.randn(E, T, generator=g, device=device)
     mu_a = torch.gather(mu, -1, actions.unsqueeze(-1)).squeeze(-1)
     term, trunc = _flags(g, E, T, p_term, p_trunc)
-    return dict(rewards=rewards.numpy(), q=q.numpy(), pi=pi.numpy(),
-                mu_a=mu_a.contiguous().numpy(),
-                actions=actions.to(torch.int32).numpy(),
-                bootstrap=bootstrap.numpy(),
-                trunc_value=trunc_value.numpy() if with_trunc else None,
+    return dict(rewards=rewards, q=q, pi=pi, mu_a=mu_a.contiguous(),
+                actions=actions.to(torch.int32), bootstrap=bootstrap,
+                trunc_value=trunc_value if with_trunc else None,
                 terminated=term, truncated=trunc if with_trunc else None)
 
 
-def forward_rollout(E: int, T: int, seed: int, p_term: float = 0.01,
-                    p_trunc: float = 0.005, with_trunc: bool = True,
-                    int_max: int = 16) -> dict:
+def forward_rollout(E: int, T: int, seed: int, p_term: float = 0.01, p_trunc: float = 0.005,
+                    with_trunc: bool = True, int_max: int = 16, device="cpu") -> dict:
     """Inputs of the forward scans (eligibility traces, episodic prefix sums).
 
     x_f32 [E,T] ~ N(0,1) (trace signal / float prefix-sum input) and
     x_i32 [E,T] ~ U{0, ..., int_max-1}.  Draw order: x_f32, x_i32, flags.
     """
-    g = _gen(seed)
-    x_f32 = torch.randn(E, T, generator=g).numpy()
-    x_i32 = torch.randint(0, int_max, (E, T), generator=g).to(torch.int32).numpy()
+    g = _gen(seed, device)
+    x_f32 = torch.randn(E, T, generator=g, device=device)
+    x_i32 = torch.randint(0, int_max, (E, T), generator=g, device=device).to(torch.int32)
     term, trunc = _flags(g, E, T, p_term, p_trunc)
     return dict(x_f32=x_f32, x_i32=x_i32, terminated=term,
                 truncated=trunc if with_trunc else None)
 
 
-def affine_rollout(E: int, T: int, seed: int, beta_lo: float = -1.0,
-                   beta_hi: float = 1.0) -> dict:
+def affine_rollout(E: int, T: int, seed: int, beta_lo: float = -1.0, beta_hi: float = 1.0,
+                   device="cpu") -> dict:
     """Inputs of the generic scan: alpha ~ N(0,1), beta ~ U(beta_lo, beta_hi),
     carry [E] ~ N(0,1); about 2% of the betas are exactly zero (resets)."""
-    g = _gen(seed)
-    alpha = torch.randn(E, T, generator=g)
-    beta = beta_lo + (beta_hi - beta_lo) * torch.rand(E, T, generator=g)
-    zero = torch.rand(E, T, generator=g) < 0.02
+    g = _gen(seed, device)
+    alpha = torch.randn(E, T, generator=g, device=device)
+    beta = beta_lo + (beta_hi - beta_lo) * torch.rand(E, T, generator=g, device=device)
+    zero = torch.rand(E, T, generator=g, device=device) < 0.02
     beta = torch.where(zero, torch.zeros_like(beta), beta)
-    carry = torch.randn(E, generator=g)
-    return dict(alpha=alpha.numpy(), beta=beta.numpy(), carry=carry.numpy())
+    carry = torch.randn(E, generator=g, device=device)
+    return dict(alpha=alpha, beta=beta, carry=carry)
 
 
 def to_time_major(a):
-    """[E, T] -> [T, E] and [E, T, A] -> [T, E, A] (contiguous); None and
-    per-environment [E] vectors pass through unchanged."""
+    """[E, T] -> [T, E] and [E, T, A] -> [T, E, A] (contiguous, numpy or
+    torch); None and per-environment [E] vectors pass through unchanged."""
     if a is None or a.ndim == 1:
         return a
+    if isinstance(a, torch.Tensor):
+        return a.transpose(0, 1).contiguous()
     if a.ndim == 2:
         return np.ascontiguousarray(a.T)
     return np.ascontiguousarray(a.transpose(1, 0, 2))

@@ -18,5 +18,6 @@ def cuda_lib():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from first_order_linear_gb300 import _lib
+    from first_order_linear_gb300 import _lib, build
+    build.build()
     return _lib.load()

@@ -1,0 +1,225 @@
+"""GPU parity: every estimator through the C ABI against the float64 oracle.
+
+Workloads follow the benchmark configurations of the rl-triton paper's
+massively parallel regime: the 8 x 16 GAE case, 4096 x 128 (GAE, discounted
+return, TD(lambda)), 4096 x 256 V-Trace, 1024 x 2048 Retrace with 18 actions,
+and the sweep of all estimators over E in {256, 1024, 4096, 16384} x
+T in {32, 128, 512, 2048}, both layouts, with and without truncation; plus
+edge cases (T = 1, ragged T, tile +- 1, E = 1, misaligned pointers, the
+two-pass path, both flags on one step, int32 wraparound).
+"""
+import numpy as np
+import pytest
+import torch
+
+from first_order_linear_gb300 import _lib, rlca, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+ESTIMATORS = ["gae", "disc", "td", "vtrace", "retrace", "elig", "psum_i32"]
+
+
+@pytest.fixture(autouse=True)
+def _gpu(cuda_lib):
+    yield
+
+
+# --------------------------------------------------------------------------
+# the named workloads
+# --------------------------------------------------------------------------
+
+def test_gae_8x16_seed0():
+    """GAE fp32, 8 envs x 16 steps, seed 0, termination 5%, truncation 2%."""
+    d = synth.value_rollout(8, 16, seed=0, p_term=0.05, p_trunc=0.02, with_trunc=True)
+    for tm in (False, True):
+        for mp in (False, True):
+            parity.check_case("gae", 8, 16, inputs=d, time_major=tm, multipass=mp)
+
+
+@pytest.mark.parametrize("kind", ["gae", "disc", "td"])
+@pytest.mark.parametrize("trunc", [True, False])
+def test_4096x128_value_estimators(kind, trunc):
+    d = synth.value_rollout(4096, 128, seed=synth.config_seed("4096x128"), p_term=0.01, p_trunc=0.005,
+                            with_trunc=trunc)
+    parity.check_case(kind, 4096, 128, inputs=d, rows=np.arange(4096))
+
+
+def test_vtrace_4096x256():
+    d = synth.vtrace_rollout(4096, 256, seed=synth.config_seed("vtrace4096x256"), p_term=0.01)
+    parity.check_case("vtrace", 4096, 256, inputs=d, rows=np.arange(4096))
+
+
+def test_retrace_1024x2048():
+    d = synth.retrace_rollout(1024, 2048, seed=synth.config_seed("retrace1024x2048"), p_term=0.002,
+                              device="cuda")
+    parity.check_case("retrace", 1024, 2048, inputs=d, rows=np.arange(1024))
+
+
+@pytest.mark.parametrize("trunc", [False, True], ids=["notrunc", "trunc"])
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
+@pytest.mark.parametrize("T", [32, 128, 512, 2048])
+@pytest.mark.parametrize("E", [256, 1024, 4096, 16384])
+@pytest.mark.parametrize("kind", ESTIMATORS)
+def test_sweep(kind, E, T, tm, trunc):
+    seed = synth.config_seed(f"sweep-{kind}-{E}-{T}-{tm}-{trunc}")
+    parity.check_case(kind, E, T, seed=seed, trunc=trunc, time_major=tm, gen_device="cuda")
+
+
+# --------------------------------------------------------------------------
+# edge cases
+# --------------------------------------------------------------------------
+
+EDGE_T = [1, 2, 3, 4, 5, 7, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257, 1023, 1025, 2047, 2049, 4095,
+          4097, 8193]
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
+@pytest.mark.parametrize("T", EDGE_T)
+def test_ragged_lengths(kind, T):
+    for E, tm, mp in ((3, False, False), (33, True, False), (5, False, True), (2, True, True)):
+        parity.check_case(kind, E, T, seed=T * 7 + E, trunc=True, time_major=tm, multipass=mp, p_term=0.05)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
+def test_single_env_and_dense_boundaries(kind):
+    parity.check_case(kind, 1, 300, seed=1, p_term=0.0)
+    parity.check_case(kind, 7, 64, seed=2, p_term=0.5)
+    parity.check_case(kind, 7, 64, seed=3, p_term=1.0)
+
+
+@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vtrace", "retrace", "elig", "psum_f32", "affine_bwd"])
+@pytest.mark.parametrize("tm", [False, True])
+def test_long_rows_few_envs_two_pass(kind, tm):
+    """Rows much longer than one tile on a handful of environments take the
+    segmented two-pass path by themselves."""
+    parity.check_case(kind, 3, 40000, seed=11, time_major=tm)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
+def test_misaligned_pointers(kind):
+    """Inputs and outputs at 4-byte (not 16-byte) offsets take the scalar
+    load path and must give the same results."""
+    E, T = 37, 96
+    d = parity.make_inputs(kind, E, T, seed=5, trunc=True, device="cuda", p_term=0.05)
+    shifted = {}
+    for k, v in d.items():
+        if isinstance(v, torch.Tensor) and v.dim() >= 2:
+            buf = torch.empty(v.numel() + 16, dtype=v.dtype, device=v.device)
+            view = buf[1:1 + v.numel()].view(v.shape)
+            view.copy_(v)
+            shifted[k] = view
+        else:
+            shifted[k] = v
+    parity.check_case(kind, E, T, inputs=shifted)
+
+
+@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vtrace", "retrace"])
+def test_termination_wins_over_truncation(kind):
+    E, T = 16, 50
+    d = parity.make_inputs(kind, E, T, seed=9, trunc=True, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(9)
+    both = torch.rand(E, T, generator=g, device="cuda") < 0.2
+    d["terminated"] = (d["terminated"].bool() | both).to(torch.uint8)
+    d["truncated"] = (d["truncated"].bool() | both).to(torch.uint8)
+    if d.get("trunc_value") is None:
+        d["trunc_value"] = torch.randn(E, T, generator=g, device="cuda")
+    parity.check_case(kind, E, T, inputs=d)
+    parity.check_case(kind, E, T, inputs=d, time_major=True)
+
+
+@pytest.mark.parametrize("exclusive", [False, True])
+@pytest.mark.parametrize("flag_is_start", [False, True])
+@pytest.mark.parametrize("kind", ["psum_i32", "psum_f32"])
+def test_prefix_sum_conventions(kind, exclusive, flag_is_start):
+    p = dict(exclusive=exclusive, flag_is_start=flag_is_start)
+    for E, T, tm, mp in ((64, 200, False, False), (64, 200, True, False), (5, 777, False, True),
+                         (9, 131, True, True)):
+        parity.check_case(kind, E, T, seed=E + T, time_major=tm, multipass=mp, params=p, p_term=0.05)
+
+
+def test_prefix_sum_int32_wraps():
+    E, T = 4, 1000
+    x = torch.full((E, T), 2 ** 30 + 12345, dtype=torch.int32, device="cuda")
+    x[1] = -(2 ** 31) + 7
+    term = torch.zeros(E, T, dtype=torch.uint8, device="cuda")
+    term[2, 500] = 1
+    d = dict(x_i32=x, x_f32=x.float(), terminated=term, truncated=None)
+    for tm in (False, True):
+        parity.check_case("psum_i32", E, T, inputs=d, time_major=tm)
+
+
+@pytest.mark.parametrize("A", [1, 2, 5, 18, 33, 64])
+def test_retrace_action_counts(A):
+    for tm in (False, True):
+        parity.check_case("retrace", 24, 160, seed=A, time_major=tm, num_actions=A, p_term=0.02)
+
+
+def test_vtrace_clipping_and_lambda():
+    p = dict(rho_bar=1.3, c_bar=0.7, vt_lambda=0.9)
+    for tm in (False, True):
+        parity.check_case("vtrace", 300, 96, seed=4, time_major=tm, params=p)
+
+
+def test_gamma_lambda_extremes():
+    for g, lam in ((0.0, 0.0), (1.0, 1.0), (0.5, 0.0), (1.0, 0.0)):
+        p = dict(gamma=g, lambda_=lam)
+        for kind in ("gae", "disc", "td", "elig"):
+            parity.check_case(kind, 50, 70, seed=8, params=p)
+
+
+# --------------------------------------------------------------------------
+# properties at full size
+# --------------------------------------------------------------------------
+
+def test_layouts_agree_full_size():
+    E, T = 4096, 512
+    for kind in ESTIMATORS:
+        d = parity.make_inputs(kind, E, T, seed=77, trunc=True, device="cuda")
+        a = parity.run_gpu(kind, d, time_major=False)
+        b = parity.run_gpu(kind, d, time_major=True)
+        for x, y in zip(a, b):
+            if x is None:
+                continue
+            if x.dtype == torch.int32:
+                assert torch.equal(x, y), kind
+            else:
+                err = ((x.double() - y.double()).abs() / (1 + y.double().abs())).max().item()
+                assert err <= 2 * parity.TOL, (kind, err)
+
+
+def test_td_lambda_equals_gae_returns_full_size():
+    d = parity.make_inputs("gae", 16384, 2048, seed=78, trunc=True, device="cuda")
+    adv, ret = parity.run_gpu("gae", d)
+    (td,) = parity.run_gpu("td", d)
+    err = ((td.double() - ret.double()).abs() / (1 + ret.double().abs())).max().item()
+    assert err <= 2 * parity.TOL
+
+
+def test_deterministic_and_stream_ordered():
+    d = parity.make_inputs("gae", 4096, 128, seed=79, trunc=True, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        a = parity.run_gpu("gae", d)
+    s.synchronize()
+    b = parity.run_gpu("gae", d)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_empty_inputs():
+    z = torch.empty(0, 16, device="cuda")
+    adv, ret = rlca.rlca_gae(z, z.clone())
+    assert adv.shape == (0, 16)
+    z2 = torch.empty(5, 0, device="cuda")
+    assert rlca.rlca_discounted_return(z2).shape == (5, 0)
+
+
+def test_workspace_sizes_consistent():
+    assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 4096, 128) == 0
+    assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 3, 40000) > 0
+    assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 64, 512, flags=_lib.RLCA_MULTIPASS) > 0
+    d = parity.make_inputs("gae", 3, 40000, seed=1, trunc=False, device="cuda")
+    with pytest.raises(ValueError):
+        rlca.rlca_gae(d["rewards"], d["values"], workspace=torch.empty(8, dtype=torch.uint8, device="cuda"))
