@@ -129,7 +129,7 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.rows_per_cta = q.block / W;
     q.tile = 4 * W;
     const int nwr = W > 32 ? W / 32 : 1;
-    q.smem = nwr > 1 ? (size_t)2 * nwr * 8 : 0;
+    q.smem = nwr > 1 ? (size_t)2 * q.rows_per_cta * nwr * 8 : 0;
     if (retrace)
       q.smem += (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
   }

@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
   constexpr int L = S::L, GW = S::GW, NWR = S::NWR;
 
   extern __shared__ __align__(16) unsigned char smem[];
-  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);  // [2][NWR] warp totals (NWR > 1)
-  unsigned char* est_smem = smem + (NWR > 1 ? 2 * NWR * sizeof(Aff<V>) : 0);
+  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);  // [2][ROWS][NWR] warp totals (NWR > 1)
+  unsigned char* est_smem = smem + (NWR > 1 ? 2 * S::ROWS * NWR * sizeof(Aff<V>) : 0);
 
   const int tid = threadIdx.x;
   const int j = tid % TPR;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
 
     Aff<V> boundary, next_carry;
     if constexpr (NWR > 1) {
-      Aff<V>* x = xw + (it & 1) * NWR;
+      Aff<V>* x = xw + ((it & 1) * S::ROWS + rloc) * NWR;
       if (lane == (BWD ? 0 : 31)) x[wr] = inc;
       __syncthreads();
       Aff<V> cc = carry;
