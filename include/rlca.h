@@ -150,6 +150,42 @@ int rlca_gae(const float *rewards, const float *values,
              rlca_stream_t stream);
 
 /*
+ * GAE with library-owned scratch, for callers that cannot allocate.
+ *
+ * The paper has no counterpart to this entry point.  It computes exactly
+ * what rlca_gae computes, with the same arguments minus the workspace, for
+ * callers that have no way to hand this library a device buffer: a plain C
+ * or Fortran host linked only against this library, a simulator callback
+ * that must not touch the device heap, a service that reserved all device
+ * memory at start-up.  When the two-pass path needs scratch, it uses one
+ * array that the library defines in device memory: RLCA_STATIC_SCRATCH_BYTES
+ * (1 MiB) on every GPU that loads the library, held until the process exits.
+ * Nothing is allocated, on the host or the device, by this call.
+ *
+ *  - The first call on a device looks up that array's device address (the
+ *    set-up); make that first call before any stream capture on the device.
+ *  - Problems whose two-pass path needs more than RLCA_STATIC_SCRATCH_BYTES
+ *    (8 bytes per row per segment; rlca_workspace_size with RLCA_EST_GAE
+ *    gives the figure) return RLCA_ERR_UNSUPPORTED and enqueue nothing;
+ *    use rlca_gae with a workspace for those.
+ *  - All calls on a device share the array and it keeps whatever the last
+ *    call left there.  No slot needs to start at zero: the first pass writes
+ *    every slot the second pass reads.  Calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on the array and give wrong
+ *    results: serialise them.
+ * Arguments, layouts, flags and errors otherwise as rlca_gae.
+ */
+#define RLCA_STATIC_SCRATCH_BYTES (1u << 20)
+
+int rlca_gae_static_scratch(const float *rewards, const float *values,
+                            const uint8_t *terminated,
+                            const uint8_t *truncated,
+                            const float *trunc_value, const float *bootstrap,
+                            float *advantages, float *returns, int64_t E,
+                            int64_t T, float gamma, float lambda,
+                            uint32_t flags, rlca_stream_t stream);
+
+/*
  * Discounted return (rl-triton §3.2: continuation split between the local
  * update and the boundary carry):
  *   G_t = r_t + gamma * G_next(t),  G_next = 0 / trunc_value[t] /
