@@ -6,8 +6,9 @@ truncation 0.5% with N(0, 1) continuation values, N(0, 1) bootstrap values,
 gamma = 0.99, lambda = 0.95 (the "thousands of environments, short
 rollouts" regime of rl-triton, arXiv:2608.17641, §6-§7).
 
-One step = one call of each of the three estimators on one batch (three
-kernel launches).  The metric is env-steps per second per estimator:
+One step = GAE, discounted returns and TD(lambda) of one batch, computed by
+one fused launch (rlca_value_targets); the three separate entry points are
+timed as well.  The metric is env-steps per second per estimator:
 3 * E * T * steps / time.  Inputs stay resident in HBM; the timed steps
 rotate over enough replicas of the batch that their footprint exceeds
 three times the L2 cache, so every step reads from DRAM.
@@ -207,9 +208,9 @@ def _kernel_source_hash():
 
 
 def _recorded_traffic():
-    """DRAM bytes per GAE launch from the committed ncu summary, if it was
+    """DRAM bytes per fused value-target launch from the committed ncu summary, if it was
     taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "gae_4096x128_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "value_targets_4096x128_traffic.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -222,6 +223,59 @@ def _recorded_traffic():
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def _calls(lib, P):
+    """The C-ABI calls of one step's estimators on a replica x and stream s."""
+    def fused(x, s):
+        return lib.rlca_value_targets(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
+                                      P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), P(x["disc"]),
+                                      P(x["td"]), E, T, GAMMA, LAMBDA, 0, None, 0, s)
+
+    def gae(x, s):
+        return lib.rlca_gae(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
+                            P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), E, T, GAMMA, LAMBDA,
+                            0, None, 0, s)
+
+    def disc(x, s):
+        return lib.rlca_discounted_return(P(x["rewards"]), P(x["terminated"]), P(x["truncated"]),
+                                          P(x["trunc_value"]), P(x["bootstrap"]), P(x["disc"]), E, T, GAMMA, 0,
+                                          None, 0, s)
+
+    def td(x, s):
+        return lib.rlca_td_lambda(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
+                                  P(x["trunc_value"]), P(x["bootstrap"]), P(x["td"]), E, T, GAMMA, LAMBDA, 0, None,
+                                  0, s)
+    return fused, gae, disc, td
+
+
+def _capture(reps, fns, stream):
+    """One CUDA graph holding, for each replica in order, the given calls."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        s = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for x in reps:
+            for f in fns:
+                st = f(x, s)
+                if st != 0:
+                    raise RuntimeError(f"capture failed with status {st}")
+    return g
+
+
+def _graph_us(g, launches, stream, replays=20):
+    """Average time per launch of a graph replayed back to back."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        a.record()
+        for _ in range(replays):
+            g.replay()
+        b.record()
+    stream.synchronize()
+    return a.elapsed_time(b) * 1e3 / (replays * launches)
 
 
 def run_ours(args):
@@ -250,74 +304,34 @@ def run_ours(args):
     reps = []
     for i in range(nb):
         x = {k: (v.clone() if v is not None else None) for k, v in d.items()}
-        x["adv"] = torch.empty(E, T, device=dev)
-        x["ret"] = torch.empty(E, T, device=dev)
-        x["disc"] = torch.empty(E, T, device=dev)
-        x["td"] = torch.empty(E, T, device=dev)
+        for k in ("adv", "ret", "disc", "td"):
+            x[k] = torch.empty(E, T, device=dev)
         reps.append(x)
     footprint = nb * (in_bytes + out_bytes)
 
     P = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    fused, gae, disc, td = _calls(lib, P)
     stream = torch.cuda.Stream(dev)
-    sptr = C.c_void_p(stream.cuda_stream)
-
-    def launch(x):
-        st = lib.rlca_gae(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                          P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), E, T, GAMMA, LAMBDA,
-                          0, None, 0, sptr)
-        st |= lib.rlca_discounted_return(P(x["rewards"]), P(x["terminated"]), P(x["truncated"]),
-                                         P(x["trunc_value"]), P(x["bootstrap"]), P(x["disc"]), E, T, GAMMA, 0,
-                                         None, 0, sptr)
-        st |= lib.rlca_td_lambda(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                                 P(x["trunc_value"]), P(x["bootstrap"]), P(x["td"]), E, T, GAMMA, LAMBDA, 0,
-                                 None, 0, sptr)
-        if st != 0:
-            raise RuntimeError(f"launch failed with status {st}")
-
-    # one CUDA graph per replica: [e0] gae [e1] discounted [e2] td(lambda) [e3]
-    try:
-        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-        mk()
-        timed_in_graph = True
-    except TypeError:
-        timed_in_graph = False
-    graphs, evs = [], []
-    with torch.cuda.stream(stream):
-        for x in reps:  # warm the launch path outside capture
-            launch(x)
+    with torch.cuda.stream(stream):  # first calls (device attribute cache) outside capture
+        for x in reps:
+            for f in (fused, gae, disc, td):
+                if f(x, C.c_void_p(stream.cuda_stream)) != 0:
+                    raise RuntimeError("launch failed")
     stream.synchronize()
-    for x in reps:
-        g = torch.cuda.CUDAGraph()
-        ev = [mk() for _ in range(4)] if timed_in_graph else None
-        with torch.cuda.graph(g, stream=stream):
-            if ev:
-                ev[0].record()
-            st = lib.rlca_gae(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                              P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), E, T, GAMMA,
-                              LAMBDA, 0, None, 0, C.c_void_p(torch.cuda.current_stream().cuda_stream))
-            if ev:
-                ev[1].record()
-            st |= lib.rlca_discounted_return(P(x["rewards"]), P(x["terminated"]), P(x["truncated"]),
-                                             P(x["trunc_value"]), P(x["bootstrap"]), P(x["disc"]), E, T, GAMMA,
-                                             0, None, 0, C.c_void_p(torch.cuda.current_stream().cuda_stream))
-            if ev:
-                ev[2].record()
-            st |= lib.rlca_td_lambda(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                                     P(x["trunc_value"]), P(x["bootstrap"]), P(x["td"]), E, T, GAMMA, LAMBDA,
-                                     0, None, 0, C.c_void_p(torch.cuda.current_stream().cuda_stream))
-            if ev:
-                ev[3].record()
-        if st != 0:
-            raise RuntimeError(f"capture failed with status {st}")
-        graphs.append(g)
-        evs.append(ev)
+
+    # the timed region: one fused launch per step, consecutive steps on
+    # consecutive replicas, captured as graphs of a full rotation (plus the
+    # remainder) and replayed back to back
+    full = _capture(reps, [fused], stream)
+    rem_n = args.steps % nb
+    rem = _capture(reps[:rem_n], [fused], stream) if rem_n else None
 
     sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "clocks.csv")
                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
     sampler.start()
     with torch.cuda.stream(stream):
-        for k in range(args.warmup):
-            graphs[k % nb].replay()
+        for _ in range(max(1, math.ceil(args.warmup / nb))):
+            full.replay()
     stream.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -328,8 +342,10 @@ def run_ours(args):
     wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         t_start.record()
-        for k in range(args.steps):
-            graphs[k % nb].replay()
+        for _ in range(args.steps // nb):
+            full.replay()
+        if rem is not None:
+            rem.replay()
         t_end.record()
     stream.synchronize()
     torch.cuda.synchronize()
@@ -345,26 +361,27 @@ def run_ours(args):
     ms_per_step = ms / args.steps
     value = world * N_EST * E * T * args.steps / (ms / 1e3)
 
-    # per-kernel durations: the last replay of each replica's graph (all inside the timed region)
-    per = None
-    if timed_in_graph and args.steps >= 1:
-        used = range(min(nb, args.steps))
-        dur = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in used] for j in range(3)]
-        per = [sum(x) / len(x) for x in dur]
-    else:
-        per = _graph_kernel_times(lib, reps, P, stream)
+    # per-kernel figures, each from a graph of one rotation of that launch
+    kern = {}
+    for name, fns in (("value_targets_fused", [fused]), ("gae", [gae]), ("discounted_return", [disc]),
+                      ("td_lambda", [td]), ("unfused_step_gae_disc_td", [gae, disc, td])):
+        g = _capture(reps, fns, stream)
+        us = _graph_us(g, nb, stream)
+        kern[name] = {"us_per_launch" if len(fns) == 1 else "us_per_step": us,
+                      "env_steps_per_s_per_estimator": (N_EST if len(fns) != 1 or name.startswith("value") else 1)
+                      * E * T / (us / 1e6)}
+        del g
     n_trunc = int(d_cpu["truncated"].sum())
-    gae_bytes = E * T * (4 + 4 + 1 + 1 + 4 + 4) + 32 * n_trunc + 4 * E
+    fused_bytes = E * T * (4 + 4 + 1 + 1 + 4 * 4) + 32 * n_trunc + 4 * E
     peak, peak_kind = _peaks()
-    achieved = gae_bytes / (per[0] / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "em_scan_kernel<GaeEst<true>,32> (rlca_gae)", "achieved": achieved,
-                "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                "traffic": _recorded_traffic(), "algorithmic_bytes_per_launch": gae_bytes,
-                "avg_launch_us": per[0] * 1e3,
-                "timing": "CUDA events recorded inside each replica's graph around the launch"
-                if timed_in_graph else "CUDA events around replays of a graph of this kernel's launches"}
-    per_est = {name: {"us_per_launch": t * 1e3, "env_steps_per_s": E * T / (t / 1e3)}
-               for name, t in zip(("gae", "discounted_return", "td_lambda"), per)}
+    avg_us = ms_per_step * 1e3
+    achieved = fused_bytes / (avg_us / 1e6) / 1e9
+    roofline = {"bound": "hbm", "kernel": "em_scan_kernel<ValueTargetsEst<true>,32> (rlca_value_targets)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "traffic": _recorded_traffic(),
+                "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_us": avg_us,
+                "timing": "timed region / steps: CUDA events on the launching stream around the K back-to-back "
+                          "launches (one launch per step)"}
 
     e2e = None if args.skip_e2e else run_e2e(args, d_cpu, dev)
     cpu = None
@@ -377,10 +394,10 @@ def run_ours(args):
                 "global_batch": world * E, "seq_len": T,
                 "l2": f"inputs rotated over {nb} replicas ({footprint / 2**20:.0f} MiB > 3 x L2 "
                       f"{l2 / 2**20:.0f} MiB); no flush",
-                "launch": "one CUDA graph per replica (3 kernels), replayed back to back"}),
+                "launch": "one fused rlca_value_targets launch per step; CUDA graphs of one rotation of "
+                          "consecutive steps, replayed back to back"}),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": N_EST * args.steps, "per_estimator": per_est,
-            "wall_s_timed_region": wall}
+            "gpu_launches": args.steps, "kernels": kern, "wall_s_timed_region": wall}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -388,46 +405,10 @@ def run_ours(args):
     return 0
 
 
-def _graph_kernel_times(lib, reps, P, stream, replays=20):
-    """Per-launch time of each estimator from a graph holding only that
-    estimator's launches (one per replica), replayed between two events."""
-    import torch
-    E_, T_ = E, T
-    calls = [
-        lambda x, s: lib.rlca_gae(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                                  P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), E_, T_,
-                                  GAMMA, LAMBDA, 0, None, 0, s),
-        lambda x, s: lib.rlca_discounted_return(P(x["rewards"]), P(x["terminated"]), P(x["truncated"]),
-                                                P(x["trunc_value"]), P(x["bootstrap"]), P(x["disc"]), E_, T_,
-                                                GAMMA, 0, None, 0, s),
-        lambda x, s: lib.rlca_td_lambda(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
-                                        P(x["trunc_value"]), P(x["bootstrap"]), P(x["td"]), E_, T_, GAMMA,
-                                        LAMBDA, 0, None, 0, s),
-    ]
-    out = []
-    for call in calls:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            s = C.c_void_p(torch.cuda.current_stream().cuda_stream)
-            for x in reps:
-                call(x, s)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            a.record()
-            for _ in range(replays):
-                g.replay()
-            b.record()
-        stream.synchronize()
-        out.append(a.elapsed_time(b) / (replays * len(reps)))
-    return out
-
-
 def run_e2e(args, d_cpu, dev):
     """Same metric through the public Python API with host buffers: every
     step copies its inputs from pinned host memory to the device, runs the
-    three estimators and copies their four outputs back."""
+    fused value-target call and copies its four outputs back."""
     import torch
     from first_order_linear_gb300 import rlca
 
@@ -443,13 +424,10 @@ def run_e2e(args, d_cpu, dev):
         for k, v in host.items():
             if v is not None:
                 devb[k].copy_(v, non_blocking=True)
-        rlca.rlca_gae(devb["rewards"], devb["values"], devb["terminated"], devb["truncated"],
-                      devb["trunc_value"], devb["bootstrap"], gamma=GAMMA, lambda_=LAMBDA,
-                      advantages=outs[0], returns=outs[1])
-        rlca.rlca_discounted_return(devb["rewards"], devb["terminated"], devb["truncated"], devb["trunc_value"],
-                                    devb["bootstrap"], gamma=GAMMA, out=outs[2])
-        rlca.rlca_td_lambda(devb["rewards"], devb["values"], devb["terminated"], devb["truncated"],
-                            devb["trunc_value"], devb["bootstrap"], gamma=GAMMA, lambda_=LAMBDA, out=outs[3])
+        rlca.rlca_value_targets(devb["rewards"], devb["values"], devb["terminated"], devb["truncated"],
+                                devb["trunc_value"], devb["bootstrap"], gamma=GAMMA, lambda_=LAMBDA,
+                                advantages=outs[0], returns=outs[1], disc_returns=outs[2],
+                                td_lambda_returns=outs[3])
         for o, b in zip(outs, back):
             b.copy_(o, non_blocking=True)
 

@@ -10,7 +10,7 @@ the seeded synthetic rollouts.
 """
 from .rlca import (  # noqa: F401
     rlca_affine_scan, rlca_discounted_return, rlca_elig_trace, rlca_episodic_prefix_sum, rlca_gae,
-    rlca_retrace, rlca_td_lambda, rlca_vtrace, rlca_workspace_size,
+    rlca_retrace, rlca_td_lambda, rlca_value_targets, rlca_vtrace, rlca_workspace_size,
 )
 
 __version__ = "0.1.0"

@@ -32,6 +32,7 @@ RLCA_EST_RETRACE = 5
 RLCA_EST_ELIG_TRACE = 6
 RLCA_EST_PREFIX_SUM = 7
 RLCA_EST_AFFINE_SCAN = 8
+RLCA_EST_VALUE_TARGETS = 9
 
 RLCA_F32 = 0
 RLCA_I32 = 1
@@ -51,6 +52,7 @@ SIGNATURES = {
     "rlca_version": (_i, []),
     "rlca_workspace_size": (_i, [_i, _i64, _i64, C.c_int32, _u32, C.POINTER(_sz)]),
     "rlca_gae": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p, _sz, _p]),
+    "rlca_value_targets": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p, _sz, _p]),
     "rlca_gae_static_scratch": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p]),
     "rlca_discounted_return": (_i, [_p, _p, _p, _p, _p, _p, _i64, _i64, _f, _u32, _p, _sz, _p]),
     "rlca_td_lambda": (_i, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p, _sz, _p]),

@@ -15,6 +15,7 @@ namespace {
 
 constexpr int64_t kMaxT = int64_t(1) << 30;
 constexpr int64_t kMaxE = INT32_MAX;
+constexpr size_t kMaxMapBytes = sizeof(Aff<F3>);  // largest affine map of any estimator
 
 int next_pow2(int64_t x) {
   int p = 1;
@@ -118,20 +119,21 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.block = 32 * C;
     q.rows_per_cta = 32;
     q.tile = 8 * C;
-    q.smem = (size_t)2 * C * 32 * 8;
-    if (retrace) q.smem += (size_t)C * 64 * num_actions * 4 + (size_t)3 * (q.tile + 1) * 32 * 4;
+    q.smem_driver_bound = (size_t)2 * C * 32 * kMaxMapBytes;
+    q.smem = retrace ? (size_t)C * 64 * num_actions * 4 + (size_t)3 * (q.tile + 1) * 32 * 4 : 0;
   } else {
     const int wmax = retrace ? kRetraceEmMaxWidth : kEmMaxWidth;
-    int W = (int)std::min<int64_t>(next_pow2(std::max<int64_t>((T + 3) / 4, kEmMinWidth)), wmax);
+    int W = (int)std::min<int64_t>(next_pow2(std::max<int64_t>((T + kEmSteps - 1) / kEmSteps, kEmMinWidth)),
+                                   wmax);
     if (flags & RLCA_MULTIPASS) W = std::max(kEmMinWidth, W / 4);
     q.width = W;
     q.block = std::max(W, 256);
     q.rows_per_cta = q.block / W;
-    q.tile = 4 * W;
+    q.tile = kEmSteps * W;
     const int nwr = W > 32 ? W / 32 : 1;
-    q.smem = nwr > 1 ? (size_t)2 * q.rows_per_cta * nwr * 8 : 0;
-    if (retrace)
-      q.smem += (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
+    q.smem_driver_bound = nwr > 1 ? (size_t)2 * q.rows_per_cta * nwr * kMaxMapBytes : 0;
+    q.smem = retrace ? (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4
+                     : 0;
   }
   q.ntiles = (int)((T + q.tile - 1) / q.tile);
   q.row_blocks = (E + q.rows_per_cta - 1) / q.rows_per_cta;
@@ -149,9 +151,11 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const int seg_tiles = (q.ntiles + nseg - 1) / nseg;
   q.seg_len = seg_tiles * q.tile;
   q.nseg = (q.ntiles + seg_tiles - 1) / seg_tiles;
-  q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * 8 : 0;
+  // one affine map per (row, segment): two values, three of each for the fused value targets
+  const size_t ws_elem = kind == Kind::ValueTargets ? 24 : 8;
+  q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
-  if (q.smem > 227 * 1024) return false;
+  if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
   *out = q;
   return true;
 }
@@ -187,6 +191,7 @@ int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions
     case RLCA_EST_ELIG_TRACE: kind = Kind::Elig; break;
     case RLCA_EST_PREFIX_SUM: kind = Kind::PrefixSum; break;
     case RLCA_EST_AFFINE_SCAN: kind = Kind::Affine; break;
+    case RLCA_EST_VALUE_TARGETS: kind = Kind::ValueTargets; break;
     default: return RLCA_ERR_INVALID_ARG;
   }
   const uint32_t allowed =
@@ -228,6 +233,39 @@ int rlca_gae(const float* rewards, const float* values, const uint8_t* terminate
   GaeEst<false> e;
   e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma; e.gl = gamma * lambda;
   return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+}
+
+int rlca_value_targets(const float* rewards, const float* values, const uint8_t* terminated,
+                       const uint8_t* truncated, const float* trunc_value, const float* bootstrap, float* advantages,
+                       float* returns, float* disc_returns, float* td_lambda_returns, int64_t E, int64_t T,
+                       float gamma, float lambda, uint32_t flags, void* workspace, size_t workspace_bytes,
+                       rlca_stream_t stream) {
+  int st;
+  if (check_sizes(E, T, &st)) return st;
+  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!rewards || !values || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
+  if (!advantages && !returns && !disc_returns && !td_lambda_returns) return RLCA_ERR_INVALID_ARG;
+  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
+                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                  {{advantages, nf}, {returns, nf}, {disc_returns, nf}, {td_lambda_returns, nf}}))
+    return RLCA_ERR_INVALID_ARG;
+  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) &&
+                   aligned(returns, 16) && aligned(disc_returns, 16) && aligned(td_lambda_returns, 16) &&
+                   aligned(terminated, 4) && aligned(truncated, 4);
+  const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
+  auto fill = [&](auto& e) {
+    e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.disc = disc_returns;
+    e.td = td_lambda_returns; e.gamma = gamma; e.gl = gamma * lambda; e.one_minus_lambda = 1.f - lambda;
+  };
+  if (truncated) {
+    ValueTargetsEst<true> e;
+    fill(e);
+    return launch(Kind::ValueTargets, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  }
+  ValueTargetsEst<false> e;
+  fill(e);
+  return launch(Kind::ValueTargets, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
 }
 
 int rlca_discounted_return(const float* rewards, const uint8_t* terminated, const uint8_t* truncated,

@@ -16,25 +16,35 @@ struct WidthCaps<RetraceEst<H>> {
   static constexpr int tm = kRetraceTmMaxWidth;
 };
 
+// smem = the driver's exchange arrays (sized here from the same shape
+// constants and map type the kernel uses) + the estimator's staging bytes
 template <class Est>
-static cudaError_t launch_one(void (*kernel)(Est, Geom), const Plan& p, const Est& est, const Geom& g,
-                              cudaStream_t s) {
-  if (p.smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+static cudaError_t launch_one(void (*kernel)(Est, Geom), const Plan& p, size_t smem, const Est& est,
+                              const Geom& g, cudaStream_t s) {
+  if (smem > kMaxSmemPerCta) return cudaErrorInvalidConfiguration;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.row_blocks * p.nseg));
   cfg.blockDim = dim3((unsigned)p.block);
-  cfg.dynamicSmemBytes = p.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, est, g);
 }
 
 template <class Est, int W>
 static cudaError_t launch_em_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if constexpr (W <= WidthCaps<Est>::em) {
-    return launch_one<Est>(em_scan_kernel<Est, W>, p, est, g, s);
+    using S = EmShape<W>;
+    const size_t drv = S::NWR > 1 ? (size_t)2 * S::ROWS * S::NWR * sizeof(Aff<typename Est::V>) : 0;
+    return launch_one<Est>(em_scan_kernel<Est, W>, p, drv + p.smem, est, g, s);
   } else {
     return cudaErrorInvalidConfiguration;
   }
@@ -43,7 +53,8 @@ static cudaError_t launch_em_w(const Plan& p, const Est& est, const Geom& g, cud
 template <class Est, int C>
 static cudaError_t launch_tm_c(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if constexpr (C <= WidthCaps<Est>::tm) {
-    return launch_one<Est>(tm_scan_kernel<Est, C>, p, est, g, s);
+    const size_t drv = (size_t)2 * C * 32 * sizeof(Aff<typename Est::V>);
+    return launch_one<Est>(tm_scan_kernel<Est, C>, p, drv + p.smem, est, g, s);
   } else {
     return cudaErrorInvalidConfiguration;
   }
@@ -63,6 +74,8 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
     }
   }
   switch (p.width) {
+    case 1: return launch_em_w<Est, 1>(p, est, g, s);
+    case 2: return launch_em_w<Est, 2>(p, est, g, s);
     case 4: return launch_em_w<Est, 4>(p, est, g, s);
     case 8: return launch_em_w<Est, 8>(p, est, g, s);
     case 16: return launch_em_w<Est, 16>(p, est, g, s);

@@ -34,7 +34,7 @@ namespace rlca {
 
 // Default no-op staging.
 struct NoStage {
-  template <int ROWS, int BLOCK, class Lay>
+  template <int ROWS, int BLOCK, int TILE, class Lay>
   __device__ __forceinline__ void stage(const Lay&, int64_t, int, int, int, unsigned char*) const {}
   template <int BLOCK, class Lay>
   __device__ __forceinline__ void stage_tm(const Lay&, int64_t, int, int, unsigned char*) const {}
@@ -108,7 +108,7 @@ struct GaeEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     load_vals<L>(r, lay, row, t0, n, vec, R.r);
     load_vals<L>(v, lay, row, t0, n, vec, R.v);
     load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
@@ -167,7 +167,7 @@ struct DiscEst : NoStage {
   }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     load_vals<L>(r, lay, row, t0, n, vec, R.r);
     load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
   }
@@ -220,7 +220,7 @@ struct TdLambdaEst : NoStage {
   }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     load_vals<L>(r, lay, row, t0, n, vec, R.r);
     load_vals<L>(v, lay, row, t0, n, vec, R.v);
     load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
@@ -249,6 +249,83 @@ struct TdLambdaEst : NoStage {
   __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
                                         bool vec) const {
     store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  }
+};
+
+// ===========================================================================
+// Fused value targets: GAE (adv, ret), discounted return and TD(lambda) of
+// one rollout from a single read of r, V and the flags.  The three
+// recurrences are the ones of GaeEst, DiscEst and TdLambdaEst, scanned side
+// by side as one F3-valued affine map per step (.x GAE, .y discounted
+// return, .z TD(lambda)); carry A_T = (0, bootstrap, bootstrap).
+// ===========================================================================
+template <bool HAS_TRUNC>
+struct ValueTargetsEst : NoStage {
+  using V = F3;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 1;
+  BoundaryArgs b;
+  const float* r;
+  const float* v;
+  float* adv;   // each output nullable
+  float* ret;
+  float* disc;
+  float* td;
+  float gamma, gl, one_minus_lambda;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], v[L], vnext;
+    float oa[L], orr[L], od[L], ot[L];
+  };
+  __device__ __forceinline__ F3 row_carry(int64_t row) const {
+    const float bb = b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
+    return F3(0.f, bb, bb);
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
+                                       int, int, int, unsigned char*) const {
+    load_vals<L>(r, lay, row, t0, n, vec, R.r);
+    load_vals<L>(v, lay, row, t0, n, vec, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+    R.vnext = 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    g[0] = __ldg(v + lay.at(row, t));
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
+  template <int L>
+  __device__ __forceinline__ Aff<F3> coef(const Regs<L>& R, int k, int t) const {
+    const bool tm = (R.bd.term >> k) & 1u, tr = (R.bd.trunc >> k) & 1u;
+    const bool last = t == b.T - 1;
+    const float v_in = (k + 1 < L) ? R.v[k + 1] : R.vnext;
+    const float vn = successor(R.bd, k, t, b.T, v_in);
+    const float delta = R.r[k] + gamma * vn - R.v[k];
+    const float a_disc = tr ? R.r[k] + gamma * R.bd.tv[k] : R.r[k];
+    const float tail = tm ? 0.f : (tr ? R.bd.tv[k] : one_minus_lambda * (last ? R.bd.boot : v_in));
+    const float a_td = R.r[k] + gamma * tail;
+    const bool c = tm || tr;
+    return {F3(delta, a_disc, a_td), F3((c || last) ? 0.f : gl, c ? 0.f : gamma, c ? 0.f : gl)};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, F3 A, F3, const Aff<F3>&) const {
+    R.oa[k] = A.x;
+    R.orr[k] = A.x + R.v[k];
+    R.od[k] = A.y;
+    R.ot[k] = A.z;
+  }
+  template <int L, class Lay>
+  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
+                                        bool vec) const {
+    if (adv != nullptr) store_vals<L>(adv, lay, row, t0, n, vec, R.oa);
+    if (ret != nullptr) store_vals<L>(ret, lay, row, t0, n, vec, R.orr);
+    if (disc != nullptr) store_vals<L>(disc, lay, row, t0, n, vec, R.od);
+    if (td != nullptr) store_vals<L>(td, lay, row, t0, n, vec, R.ot);
   }
 };
 
@@ -283,7 +360,7 @@ struct VtraceEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     float a[L], bb[L];
     load_vals<L>(r, lay, row, t0, n, vec, R.r);
     load_vals<L>(v, lay, row, t0, n, vec, R.v);
@@ -398,11 +475,11 @@ struct RetraceEst {
 
   // shared memory: per warp raw Q and pi blocks [32 * A] each, then the
   // staged per-step scalars [3][ROWS][tile + 1]
-  template <int ROWS, int BLOCK, class Lay>
+  template <int ROWS, int BLOCK, int TILE, class Lay>
   __device__ __forceinline__ void stage(const Lay& lay, int64_t row0, int, int ts, int te,
                                         unsigned char* sm) const {
     constexpr int NW = BLOCK / 32;
-    constexpr int SROW = 4 * (BLOCK / ROWS) + 1;  // tile + 1 steps per row
+    constexpr int SROW = TILE + 1;  // tile + 1 steps per row
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* raw_q = reinterpret_cast<float*>(sm) + warp * 64 * st.A;
@@ -443,14 +520,14 @@ struct RetraceEst {
 
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int slot, int t0, int n,
-                                       bool vec, int ts, int tile, unsigned char* sm) const {
+                                       bool vec, int ts, int tile, int nrows, unsigned char* sm) const {
     load_vals<L>(r, lay, row, t0, n, vec, R.r);
     load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
     constexpr bool kTM = Lay::kTimeMajor;
     const int NW = blockDim.x >> 5;
     const float* s_ev = reinterpret_cast<const float*>(sm) + NW * 64 * st.A;
     const int srows = tile + 1;
-    const int plane = kTM ? srows * 32 : srows * (int)(blockDim.x / (tile / 4));
+    const int plane = srows * nrows;
     const float* s_qa = s_ev + plane;
     const float* s_c = s_qa + plane;
 #pragma unroll
@@ -518,7 +595,7 @@ struct EligEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     load_vals<L>(x, lay, row, t0, n, vec, R.x);
     R.done = load_flags<L>(term, lay, row, t0, n, vec) | load_flags<L>(trunc, lay, row, t0, n, vec);
     R.prev_done = 1.f;
@@ -578,7 +655,7 @@ struct PrefixSumEst : NoStage {
   __device__ __forceinline__ V row_carry(int64_t) const { return V(0); }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     if constexpr (std::is_integral<V>::value) {
       load_ints<L>(static_cast<const int32_t*>(x), lay, row, t0, n, vec, R.x);
     } else {
@@ -643,7 +720,7 @@ struct AffineEst : NoStage {
   }
   template <int L, class Lay>
   __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, unsigned char*) const {
+                                       int, int, int, unsigned char*) const {
     load_vals<L>(alpha, lay, row, t0, n, vec, R.a);
     load_vals<L>(beta, lay, row, t0, n, vec, R.b);
   }

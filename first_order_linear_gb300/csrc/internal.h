@@ -9,7 +9,7 @@
 
 namespace rlca {
 
-enum class Kind { Gae, Disc, TdLambda, Vtrace, Retrace, Elig, PrefixSum, Affine };
+enum class Kind { Gae, Disc, TdLambda, Vtrace, Retrace, Elig, PrefixSum, Affine, ValueTargets };
 
 // Largest env-major threads-per-row and time-major chunk-threads per
 // environment of a kind (Retrace keeps its tiles small: it stages its
@@ -18,7 +18,8 @@ constexpr int kEmMaxWidth = 1024;
 constexpr int kTmMaxWidth = 32;
 constexpr int kRetraceEmMaxWidth = 256;
 constexpr int kRetraceTmMaxWidth = 8;
-constexpr int kEmMinWidth = 4;
+constexpr int kEmMinWidth = 1;
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 struct Plan {
   bool time_major;
@@ -30,7 +31,8 @@ struct Plan {
   int nseg;         // segments per row (> 1: two-pass)
   int seg_len;      // steps per segment
   int64_t row_blocks;
-  size_t smem;      // dynamic shared memory per CTA
+  size_t smem;      // estimator staging shared memory per CTA (the launcher adds the driver's exchange arrays)
+  size_t smem_driver_bound;  // upper bound of the driver's part, for the size check
   size_t ws_bytes;  // workspace of the two-pass path
 };
 

@@ -1,4 +1,5 @@
-// Kernels of the value-target estimators: GAE, discounted return, TD(lambda).
+// Kernels of the value-target estimators: GAE, discounted return, TD(lambda),
+// and the fused pass computing all three.
 #include "dispatch.cuh"
 
 namespace rlca {
@@ -9,4 +10,8 @@ template cudaError_t run_scan<DiscEst<false>>(const DiscEst<false>&, const Plan&
 template cudaError_t run_scan<TdLambdaEst<true>>(const TdLambdaEst<true>&, const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<TdLambdaEst<false>>(const TdLambdaEst<false>&, const Plan&, const Geom&,
                                                   cudaStream_t);
+template cudaError_t run_scan<ValueTargetsEst<true>>(const ValueTargetsEst<true>&, const Plan&, const Geom&,
+                                                     cudaStream_t);
+template cudaError_t run_scan<ValueTargetsEst<false>>(const ValueTargetsEst<false>&, const Plan&, const Geom&,
+                                                      cudaStream_t);
 }  // namespace rlca

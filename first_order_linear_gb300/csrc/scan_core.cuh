@@ -47,17 +47,47 @@ __device__ __forceinline__ Aff<V> compose(const Aff<V>& outer, const Aff<V>& inn
   return {outer.a + outer.b * inner.a, outer.b * inner.b};
 }
 
+// Three independent recurrences scanned side by side (the fused value-target
+// scan: GAE, discounted return and TD(lambda) of one row).  Arithmetic is
+// element-wise, so compose() on Aff<F3> composes the three maps at once.
+struct F3 {
+  float x, y, z;
+  __host__ __device__ F3() = default;
+  __host__ __device__ constexpr F3(float s) : x(s), y(s), z(s) {}
+  __host__ __device__ constexpr F3(float a, float b, float c) : x(a), y(b), z(c) {}
+};
+__device__ __forceinline__ F3 operator+(const F3& a, const F3& b) { return {a.x + b.x, a.y + b.y, a.z + b.z}; }
+__device__ __forceinline__ F3 operator*(const F3& a, const F3& b) { return {a.x * b.x, a.y * b.y, a.z * b.z}; }
+
+__device__ __forceinline__ float shfl_down_v(float v, int d, int w) { return __shfl_down_sync(kFullMask, v, d, w); }
+__device__ __forceinline__ uint32_t shfl_down_v(uint32_t v, int d, int w) {
+  return __shfl_down_sync(kFullMask, v, d, w);
+}
+__device__ __forceinline__ F3 shfl_down_v(const F3& v, int d, int w) {
+  return {shfl_down_v(v.x, d, w), shfl_down_v(v.y, d, w), shfl_down_v(v.z, d, w)};
+}
+__device__ __forceinline__ float shfl_up_v(float v, int d, int w) { return __shfl_up_sync(kFullMask, v, d, w); }
+__device__ __forceinline__ uint32_t shfl_up_v(uint32_t v, int d, int w) { return __shfl_up_sync(kFullMask, v, d, w); }
+__device__ __forceinline__ F3 shfl_up_v(const F3& v, int d, int w) {
+  return {shfl_up_v(v.x, d, w), shfl_up_v(v.y, d, w), shfl_up_v(v.z, d, w)};
+}
+__device__ __forceinline__ float shfl_idx_v(float v, int s, int w) { return __shfl_sync(kFullMask, v, s, w); }
+__device__ __forceinline__ uint32_t shfl_idx_v(uint32_t v, int s, int w) { return __shfl_sync(kFullMask, v, s, w); }
+__device__ __forceinline__ F3 shfl_idx_v(const F3& v, int s, int w) {
+  return {shfl_idx_v(v.x, s, w), shfl_idx_v(v.y, s, w), shfl_idx_v(v.z, s, w)};
+}
+
 template <class V>
 __device__ __forceinline__ Aff<V> shfl_down_aff(const Aff<V>& x, int d, int w) {
-  return {__shfl_down_sync(kFullMask, x.a, d, w), __shfl_down_sync(kFullMask, x.b, d, w)};
+  return {shfl_down_v(x.a, d, w), shfl_down_v(x.b, d, w)};
 }
 template <class V>
 __device__ __forceinline__ Aff<V> shfl_up_aff(const Aff<V>& x, int d, int w) {
-  return {__shfl_up_sync(kFullMask, x.a, d, w), __shfl_up_sync(kFullMask, x.b, d, w)};
+  return {shfl_up_v(x.a, d, w), shfl_up_v(x.b, d, w)};
 }
 template <class V>
 __device__ __forceinline__ Aff<V> shfl_idx_aff(const Aff<V>& x, int src, int w) {
-  return {__shfl_sync(kFullMask, x.a, src, w), __shfl_sync(kFullMask, x.b, src, w)};
+  return {shfl_idx_v(x.a, src, w), shfl_idx_v(x.b, src, w)};
 }
 
 // ---------------------------------------------------------------------------
@@ -179,6 +209,18 @@ __device__ __forceinline__ void store_ints(int32_t* __restrict__ p, const Lay& l
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: the launches carry the programmatic stream
+// serialization attribute, so a kernel may be scheduled while the previous
+// kernel of the stream drains.  pdl_wait() blocks until that kernel has
+// completed and its writes are visible (no-op when launched without the
+// attribute); it comes before the first global access.  pdl_trigger() lets
+// the next kernel of the stream start launching once every CTA of this grid
+// has issued it (or exited).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // launch geometry
 // ---------------------------------------------------------------------------
 enum : int { kModeFull = 0, kModeAggregate = 1 };
@@ -194,10 +236,17 @@ struct Geom {
   void* ws;     // [E][nseg] affine maps of the segments (two-pass path)
 };
 
-// env-major: TPR threads per row, 4 steps per thread, rows packed 256 threads per CTA
+// consecutive steps per thread in the env-major driver (a multiple of 4:
+// every 4 steps are one 16-byte vector of each float input)
+#ifndef RLCA_EM_STEPS
+#define RLCA_EM_STEPS 4
+#endif
+constexpr int kEmSteps = RLCA_EM_STEPS;
+
+// env-major: TPR threads per row, kEmSteps steps per thread, rows packed 256 threads per CTA
 template <int TPR>
 struct EmShape {
-  static constexpr int L = 4;
+  static constexpr int L = kEmSteps;
   static constexpr int TILE = TPR * L;
   static constexpr int BLOCK = TPR >= 256 ? TPR : 256;
   static constexpr int ROWS = BLOCK / TPR;
@@ -259,6 +308,7 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
   const bool vec = g.vec != 0;
   const bool agg_mode = g.mode == kModeAggregate;
   const EnvMajor lay{g.E, g.T};
+  pdl_wait();
 
   Aff<V> carry;
   if (agg_mode) {
@@ -277,9 +327,10 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
     const int t0 = ts + j * L;
     const int n = row_ok ? max(0, min(L, te - t0)) : 0;
 
-    est.template stage<S::ROWS, S::BLOCK>(lay, row0, rloc, ts, te, est_smem);
+    est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, ts, te, est_smem);
     typename Est::template Regs<L> R;
-    est.template load<L>(R, lay, row, rloc, t0, n, vec, ts, S::TILE, est_smem);
+    est.template load<L>(R, lay, row, rloc, t0, n, vec, ts, S::TILE, S::ROWS, est_smem);
+    if (it == ntiles - 1) pdl_trigger();
 
     if constexpr (Est::kNb > 0) {
       // neighbour step's inputs: from the adjacent lane when it holds them,
@@ -398,6 +449,7 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
   const int seg_hi = min(g.T, seg_lo + g.seg_len);
   const bool agg_mode = g.mode == kModeAggregate;
   const TimeMajor lay{g.E, g.T};
+  pdl_wait();
 
   Aff<V> carry;
   if (agg_mode) {
@@ -418,7 +470,8 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 
     est.template stage_tm<S::BLOCK>(lay, row0, ts, te, est_smem);
     typename Est::template Regs<L> R;
-    est.template load<L>(R, lay, row, lane, t0, n, false, ts, S::TILE, est_smem);
+    est.template load<L>(R, lay, row, lane, t0, n, false, ts, S::TILE, 32, est_smem);
+    if (it == ntiles - 1) pdl_trigger();
     if constexpr (Est::kNb > 0) {
       float got[Est::kNb > 0 ? Est::kNb : 1];
 #pragma unroll

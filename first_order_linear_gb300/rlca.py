@@ -19,7 +19,7 @@ from . import _lib
 from ._lib import check
 
 __all__ = [
-    "rlca_gae", "rlca_discounted_return", "rlca_td_lambda", "rlca_vtrace", "rlca_retrace",
+    "rlca_gae", "rlca_value_targets", "rlca_discounted_return", "rlca_td_lambda", "rlca_vtrace", "rlca_retrace",
     "rlca_elig_trace", "rlca_episodic_prefix_sum", "rlca_affine_scan", "rlca_workspace_size",
 ]
 
@@ -119,6 +119,38 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
             _ptr(rewards), _ptr(values), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap),
             _ptr(advantages), _ptr(returns), E, T, gamma, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
     return advantages, returns
+
+
+def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
+                       gamma=0.99, lambda_=0.95, advantages=None, returns=None, disc_returns=None,
+                       td_lambda_returns=None, outputs=("advantages", "returns", "disc_returns", "td_lambda_returns"),
+                       time_major=False, multipass=False, workspace=None, stream=None):
+    """GAE advantages and returns, discounted returns and TD(lambda) returns
+    in one fused pass.  ``outputs`` names the results to compute (buffers
+    passed explicitly are always written).  Returns the four tensors (None
+    for those not computed) in the order (advantages, returns,
+    disc_returns, td_lambda_returns)."""
+    lib = _lib.load()
+    dev = rewards.device
+    E, T = _dims(rewards, time_major)
+    shape = tuple(rewards.shape)
+    _check(rewards, "rewards", _F, shape, dev)
+    _check(values, "values", _F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    bufs = dict(advantages=advantages, returns=returns, disc_returns=disc_returns,
+                td_lambda_returns=td_lambda_returns)
+    for name in bufs:
+        if bufs[name] is None and name in outputs:
+            bufs[name] = torch.empty(shape, dtype=torch.float32, device=dev)
+        _check(bufs[name], name, _F, shape, dev, required=False)
+    flags = _flags(time_major, multipass)
+    with torch.cuda.device(dev):
+        ws, wsb = _workspace(_lib.RLCA_EST_VALUE_TARGETS, E, T, 0, flags, dev, workspace)
+        check("rlca_value_targets", lib.rlca_value_targets(
+            _ptr(rewards), _ptr(values), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap),
+            _ptr(bufs["advantages"]), _ptr(bufs["returns"]), _ptr(bufs["disc_returns"]),
+            _ptr(bufs["td_lambda_returns"]), E, T, gamma, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
+    return bufs["advantages"], bufs["returns"], bufs["disc_returns"], bufs["td_lambda_returns"]
 
 
 def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,

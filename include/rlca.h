@@ -38,7 +38,10 @@
  *  - Sizes: 0 <= E <= 2^31-1, 0 <= T <= 2^30.
  *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *    call returns without synchronising.  No host or device memory is
- *    allocated by any entry point.
+ *    allocated by any entry point.  Kernels are launched with programmatic
+ *    stream serialization: they may be scheduled while the previous kernel
+ *    of the stream drains, but touch no memory before it has completed, so
+ *    stream order is kept.
  *  - Workspace: an entry point may need device scratch for the two-pass
  *    segmented path (long rows on few environments, or RLCA_MULTIPASS).
  *    Query its size with rlca_workspace_size() using the same E, T,
@@ -99,6 +102,7 @@ typedef struct CUstream_st *rlca_stream_t;
 #define RLCA_EST_ELIG_TRACE        6
 #define RLCA_EST_PREFIX_SUM        7
 #define RLCA_EST_AFFINE_SCAN       8
+#define RLCA_EST_VALUE_TARGETS     9
 
 /* ---- prefix-sum element types ------------------------------------------- */
 #define RLCA_F32 0
@@ -148,6 +152,30 @@ int rlca_gae(const float *rewards, const float *values,
              int64_t E, int64_t T, float gamma, float lambda,
              uint32_t flags, void *workspace, size_t workspace_bytes,
              rlca_stream_t stream);
+
+/*
+ * Fused value targets: GAE advantages and returns, discounted returns and
+ * TD(lambda) returns of the same rollout in one pass that reads rewards,
+ * values and flags once (the three recurrences of rlca_gae,
+ * rlca_discounted_return and rlca_td_lambda, scanned side by side; rl-triton
+ * §4 Fusion: constructing coefficients on chip removes intermediate HBM
+ * round trips).  Results equal those of the three separate calls (the
+ * floating-point grouping may differ within rounding).
+ *   rewards, values, terminated, truncated, trunc_value, bootstrap  as rlca_gae
+ *   advantages, returns        [E,T] f32 outputs of rlca_gae, each nullable
+ *   disc_returns               [E,T] f32 output of rlca_discounted_return, nullable
+ *   td_lambda_returns          [E,T] f32 output of rlca_td_lambda, nullable
+ * At least one output must be given.  Workspace (two-pass path): 24 bytes
+ * per row per segment (rlca_workspace_size with RLCA_EST_VALUE_TARGETS).
+ */
+int rlca_value_targets(const float *rewards, const float *values,
+                       const uint8_t *terminated, const uint8_t *truncated,
+                       const float *trunc_value, const float *bootstrap,
+                       float *advantages, float *returns, float *disc_returns,
+                       float *td_lambda_returns, int64_t E, int64_t T,
+                       float gamma, float lambda, uint32_t flags,
+                       void *workspace, size_t workspace_bytes,
+                       rlca_stream_t stream);
 
 /*
  * GAE with library-owned scratch, for callers that cannot allocate.

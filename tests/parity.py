@@ -62,11 +62,12 @@ def _back(t, time_major):
     return synth.from_time_major(t) if time_major else t
 
 
-KINDS = ["gae", "disc", "td", "vtrace", "retrace", "elig", "psum_i32", "psum_f32", "affine_bwd", "affine_fwd"]
+KINDS = ["gae", "disc", "td", "vt", "vtrace", "retrace", "elig", "psum_i32", "psum_f32", "affine_bwd",
+         "affine_fwd"]
 
 
 def make_inputs(kind, E, T, seed, trunc, device, **kw):
-    if kind in ("gae", "disc", "td"):
+    if kind in ("gae", "disc", "td", "vt"):
         return synth.value_rollout(E, T, seed, p_term=kw.get("p_term", 0.01), p_trunc=kw.get("p_trunc", 0.005),
                                    with_trunc=trunc, device=device)
     if kind == "vtrace":
@@ -93,6 +94,9 @@ def run_gpu(kind, d, time_major=False, multipass=False, params=None):
     if kind == "gae":
         out = rlca.rlca_gae(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
                             x["bootstrap"], gamma=p["gamma"], lambda_=p["lambda_"], **common)
+    elif kind == "vt":
+        out = rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
+                                      x["bootstrap"], gamma=p["gamma"], lambda_=p["lambda_"], **common)
     elif kind == "disc":
         out = (rlca.rlca_discounted_return(x["rewards"], x["terminated"], x["truncated"], x["trunc_value"],
                                            x["bootstrap"], gamma=p["gamma"], **common),)
@@ -131,6 +135,14 @@ def run_oracle(kind, d, rows, params=None):
     if kind == "gae":
         return ref.gae(n["rewards"], n["values"], n["terminated"], n["truncated"], n["trunc_value"], n["bootstrap"],
                        gamma=g, lam=lam)
+    if kind == "vt":
+        adv, ret = ref.gae(n["rewards"], n["values"], n["terminated"], n["truncated"], n["trunc_value"],
+                           n["bootstrap"], gamma=g, lam=lam)
+        disc = ref.discounted_return(n["rewards"], n["terminated"], n["truncated"], n["trunc_value"],
+                                     n["bootstrap"], gamma=g)
+        td = ref.td_lambda(n["rewards"], n["values"], n["terminated"], n["truncated"], n["trunc_value"],
+                           n["bootstrap"], gamma=g, lam=lam)
+        return adv, ret, disc, td
     if kind == "disc":
         return (ref.discounted_return(n["rewards"], n["terminated"], n["truncated"], n["trunc_value"],
                                       n["bootstrap"], gamma=g),)

@@ -18,6 +18,7 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 ESTIMATORS = ["gae", "disc", "td", "vtrace", "retrace", "elig", "psum_i32"]
+SWEEP = ESTIMATORS + ["vt"]
 
 
 @pytest.fixture(autouse=True)
@@ -37,7 +38,7 @@ def test_gae_8x16_seed0():
             parity.check_case("gae", 8, 16, inputs=d, time_major=tm, multipass=mp)
 
 
-@pytest.mark.parametrize("kind", ["gae", "disc", "td"])
+@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vt"])
 @pytest.mark.parametrize("trunc", [True, False])
 def test_4096x128_value_estimators(kind, trunc):
     d = synth.value_rollout(4096, 128, seed=synth.config_seed("4096x128"), p_term=0.01, p_trunc=0.005,
@@ -60,7 +61,7 @@ def test_retrace_1024x2048():
 @pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
 @pytest.mark.parametrize("T", [32, 128, 512, 2048])
 @pytest.mark.parametrize("E", [256, 1024, 4096, 16384])
-@pytest.mark.parametrize("kind", ESTIMATORS)
+@pytest.mark.parametrize("kind", SWEEP)
 def test_sweep(kind, E, T, tm, trunc):
     seed = synth.config_seed(f"sweep-{kind}-{E}-{T}-{tm}-{trunc}")
     parity.check_case(kind, E, T, seed=seed, trunc=trunc, time_major=tm, gen_device="cuda")
@@ -88,7 +89,8 @@ def test_single_env_and_dense_boundaries(kind):
     parity.check_case(kind, 7, 64, seed=3, p_term=1.0)
 
 
-@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vtrace", "retrace", "elig", "psum_f32", "affine_bwd"])
+@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vt", "vtrace", "retrace", "elig", "psum_f32",
+                                  "affine_bwd"])
 @pytest.mark.parametrize("tm", [False, True])
 def test_long_rows_few_envs_two_pass(kind, tm):
     """Rows much longer than one tile on a handful of environments take the
@@ -114,7 +116,7 @@ def test_misaligned_pointers(kind):
     parity.check_case(kind, E, T, inputs=shifted)
 
 
-@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vtrace", "retrace"])
+@pytest.mark.parametrize("kind", ["gae", "disc", "td", "vt", "vtrace", "retrace"])
 def test_termination_wins_over_truncation(kind):
     E, T = 16, 50
     d = parity.make_inputs(kind, E, T, seed=9, trunc=True, device="cuda")
@@ -164,7 +166,7 @@ def test_vtrace_clipping_and_lambda():
 def test_gamma_lambda_extremes():
     for g, lam in ((0.0, 0.0), (1.0, 1.0), (0.5, 0.0), (1.0, 0.0)):
         p = dict(gamma=g, lambda_=lam)
-        for kind in ("gae", "disc", "td", "elig"):
+        for kind in ("gae", "disc", "td", "vt", "elig"):
             parity.check_case(kind, 50, 70, seed=8, params=p)
 
 
@@ -186,6 +188,15 @@ def test_layouts_agree_full_size():
             else:
                 err = ((x.double() - y.double()).abs() / (1 + y.double().abs())).max().item()
                 assert err <= 2 * parity.TOL, (kind, err)
+
+
+def test_fused_value_targets_match_separate_calls_full_size():
+    d = parity.make_inputs("gae", 16384, 2048, seed=80, trunc=True, device="cuda")
+    fused = parity.run_gpu("vt", d)
+    sep = parity.run_gpu("gae", d) + parity.run_gpu("disc", d) + parity.run_gpu("td", d)
+    for a, b in zip(fused, sep):
+        err = ((a.double() - b.double()).abs() / (1 + b.double().abs())).max().item()
+        assert err <= 2 * parity.TOL
 
 
 def test_td_lambda_equals_gae_returns_full_size():
@@ -220,6 +231,8 @@ def test_workspace_sizes_consistent():
     assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 4096, 128) == 0
     assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 3, 40000) > 0
     assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 64, 512, flags=_lib.RLCA_MULTIPASS) > 0
+    assert rlca.rlca_workspace_size(_lib.RLCA_EST_VALUE_TARGETS, 3, 40000) == \
+        3 * rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 3, 40000)
     d = parity.make_inputs("gae", 3, 40000, seed=1, trunc=False, device="cuda")
     with pytest.raises(ValueError):
         rlca.rlca_gae(d["rewards"], d["values"], workspace=torch.empty(8, dtype=torch.uint8, device="cuda"))
