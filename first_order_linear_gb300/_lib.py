@@ -23,6 +23,7 @@ RLCA_TIME_MAJOR = 0x1
 RLCA_MULTIPASS = 0x2
 RLCA_PSUM_EXCLUSIVE = 0x4
 RLCA_PSUM_FLAG_IS_START = 0x8
+RLCA_INPUTS_READY = 0x10
 
 RLCA_EST_GAE = 1
 RLCA_EST_DISCOUNTED_RETURN = 2

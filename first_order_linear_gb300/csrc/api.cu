@@ -84,7 +84,7 @@ int check_sizes(int64_t E, int64_t T, int* status) {
 
 bool flags_ok(uint32_t flags, uint32_t allowed) { return (flags & ~allowed) == 0u; }
 
-constexpr uint32_t kLayoutFlags = RLCA_TIME_MAJOR | RLCA_MULTIPASS;
+constexpr uint32_t kLayoutFlags = RLCA_TIME_MAJOR | RLCA_MULTIPASS | RLCA_INPUTS_READY;
 
 template <class Est>
 int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flags, void* ws, size_t ws_bytes,
@@ -101,6 +101,7 @@ int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flag
   g.nseg = p.nseg;
   g.mode = kModeFull;
   g.vec = (!p.time_major && vec_ok && T % 4 == 0) ? 1 : 0;
+  g.early = (flags & RLCA_INPUTS_READY) ? 1 : 0;
   g.ws = ws;
   return run_scan(est, p, g, s) == cudaSuccess ? RLCA_OK : RLCA_ERR_CUDA;
 }

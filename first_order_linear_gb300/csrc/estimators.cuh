@@ -62,8 +62,12 @@ __device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryReg
   R.term = load_flags<L>(b.term, lay, row, t0, n, vec);
   R.trunc = HAS_TRUNC ? (load_flags<L>(b.trunc, lay, row, t0, n, vec) & ~R.term) : 0u;
 #pragma unroll
-  for (int k = 0; k < L; ++k)
-    R.tv[k] = (HAS_TRUNC && ((R.trunc >> k) & 1u)) ? __ldg(b.tv + lay.at(row, t0 + k)) : 0.f;
+  for (int k = 0; k < L; ++k) R.tv[k] = 0.f;
+  if (HAS_TRUNC && R.trunc != 0u) {  // truncations are rare: one branch instead of L predicated loads
+#pragma unroll
+    for (int k = 0; k < L; ++k)
+      if ((R.trunc >> k) & 1u) R.tv[k] = __ldg(b.tv + lay.at(row, t0 + k));
+  }
   R.boot = (n > 0 && t0 + n == b.T && b.boot != nullptr) ? __ldg(b.boot + row) : 0.f;
 }
 

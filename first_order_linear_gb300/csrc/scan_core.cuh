@@ -159,9 +159,11 @@ __device__ __forceinline__ uint32_t load_flags(const uint8_t* __restrict__ p, co
     const uint32_t* q = reinterpret_cast<const uint32_t*>(p + lay.at(row, t0));
 #pragma unroll
     for (int i = 0; i < L / 4; ++i) {
-      uint32_t w = (4 * i < n) ? __ldg(q + i) : 0u;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) bits |= (((w >> (8 * k)) & 0xffu) != 0u ? 1u : 0u) << (4 * i + k);
+      const uint32_t w = (4 * i < n) ? __ldg(q + i) : 0u;
+      // one bit per nonzero byte: bytes -> 0/1, then the multiply gathers
+      // byte k's bit into bit 24 + k (the partial products never overlap)
+      const uint32_t m = __vcmpne4(w, 0u) & 0x01010101u;
+      bits |= ((m * 0x01020408u) >> 24) << (4 * i);
     }
   } else {
 #pragma unroll
@@ -233,6 +235,8 @@ struct Geom {
   int nseg;     // segments per row; > 1 selects the two-pass path
   int mode;     // kModeFull or kModeAggregate (first pass of the two-pass path)
   int vec;      // env-major only: 16-byte aligned rows, T % 4 == 0
+  int early;    // inputs do not depend on the previous kernel of the stream: load
+                // before waiting on it, wait only before the first global write
   void* ws;     // [E][nseg] affine maps of the segments (two-pass path)
 };
 
@@ -299,8 +303,8 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
   const int lane = tid & 31;
   const int lig = j % GW;
   const int wr = j / 32;
-  const int seg = blockIdx.x % g.nseg;
-  const int64_t row0 = (int64_t)(blockIdx.x / g.nseg) * S::ROWS;
+  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
+  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * S::ROWS;
   const int64_t row = row0 + rloc;
   const bool row_ok = row < g.E;
   const int seg_lo = seg * g.seg_len;
@@ -308,7 +312,8 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
   const bool vec = g.vec != 0;
   const bool agg_mode = g.mode == kModeAggregate;
   const EnvMajor lay{g.E, g.T};
-  pdl_wait();
+  const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
+  if (!early) pdl_wait();
 
   Aff<V> carry;
   if (agg_mode) {
@@ -417,6 +422,7 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
           est.emit(R, k, A, adj, c[k]);
         }
       }
+      if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
       est.template store<L>(R, lay, row, t0, n, vec);
     }
     carry = next_carry;
@@ -441,15 +447,16 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 
   const int lane = threadIdx.x & 31;
   const int cw = threadIdx.x >> 5;  // chunk index inside the tile
-  const int seg = blockIdx.x % g.nseg;
-  const int64_t row0 = (int64_t)(blockIdx.x / g.nseg) * S::EW;
+  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
+  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * S::EW;
   const int64_t row = row0 + lane;
   const bool row_ok = row < g.E;
   const int seg_lo = seg * g.seg_len;
   const int seg_hi = min(g.T, seg_lo + g.seg_len);
   const bool agg_mode = g.mode == kModeAggregate;
   const TimeMajor lay{g.E, g.T};
-  pdl_wait();
+  const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
+  if (!early) pdl_wait();
 
   Aff<V> carry;
   if (agg_mode) {
@@ -528,6 +535,7 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
           est.emit(R, k, A, adj, c[k]);
         }
       }
+      if (early && it == 0) pdl_wait();
       est.template store<L>(R, lay, row, t0, n, false);
     }
     carry = cc;

@@ -92,6 +92,7 @@ extern "C" int rlca_gae_static_scratch(const float* rewards, const float* values
   g.nseg = p.nseg;
   g.mode = kModeFull;
   g.vec = (!p.time_major && vec && T % 4 == 0) ? 1 : 0;
+  g.early = 0;
   g.ws = ws;
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
   cudaError_t e;

@@ -6,7 +6,9 @@ Each wrapper checks dtypes, devices and contiguity, allocates the outputs
 here; a missing library raises (see :func:`first_order_linear_gb300._lib.load`).
 
 Layout: env-major ``[E, T]`` by default; ``time_major=True`` takes ``[T, E]``
-(and ``[T, E, A]`` for Retrace's per-action tensors).  Flags may be uint8 or
+(and ``[T, E, A]`` for Retrace's per-action tensors).  ``inputs_ready=True``
+sets RLCA_INPUTS_READY (the inputs were not written by the kernel just before
+this call on the stream, so the call may overlap it).  Flags may be uint8 or
 bool tensors; ``None`` means "no such flag" for the optional inputs.
 """
 from __future__ import annotations
@@ -50,8 +52,9 @@ _U8 = (torch.uint8, torch.bool)
 _I32 = (torch.int32,)
 
 
-def _flags(time_major, multipass, extra=0):
-    return (_lib.RLCA_TIME_MAJOR if time_major else 0) | (_lib.RLCA_MULTIPASS if multipass else 0) | extra
+def _flags(time_major, multipass, extra=0, inputs_ready=False):
+    return ((_lib.RLCA_TIME_MAJOR if time_major else 0) | (_lib.RLCA_MULTIPASS if multipass else 0)
+            | (_lib.RLCA_INPUTS_READY if inputs_ready else 0) | extra)
 
 
 def _dims(x, time_major):
@@ -95,7 +98,7 @@ def _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E):
 
 def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
              gamma=0.99, lambda_=0.95, advantages=None, returns=None, want_returns=True,
-             time_major=False, multipass=False, workspace=None, stream=None):
+             time_major=False, multipass=False, inputs_ready=False, workspace=None, stream=None):
     """GAE advantages (and returns = advantages + values).  Returns
     ``(advantages, returns)``; returns is None when ``want_returns`` is
     False and no buffer is given."""
@@ -112,7 +115,7 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
         returns = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(advantages, "advantages", _F, shape, dev)
     _check(returns, "returns", _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_GAE, E, T, 0, flags, dev, workspace)
         check("rlca_gae", lib.rlca_gae(
@@ -124,7 +127,7 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
 def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
                        gamma=0.99, lambda_=0.95, advantages=None, returns=None, disc_returns=None,
                        td_lambda_returns=None, outputs=("advantages", "returns", "disc_returns", "td_lambda_returns"),
-                       time_major=False, multipass=False, workspace=None, stream=None):
+                       time_major=False, multipass=False, inputs_ready=False, workspace=None, stream=None):
     """GAE advantages and returns, discounted returns and TD(lambda) returns
     in one fused pass.  ``outputs`` names the results to compute (buffers
     passed explicitly are always written).  Returns the four tensors (None
@@ -143,7 +146,7 @@ def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_v
         if bufs[name] is None and name in outputs:
             bufs[name] = torch.empty(shape, dtype=torch.float32, device=dev)
         _check(bufs[name], name, _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VALUE_TARGETS, E, T, 0, flags, dev, workspace)
         check("rlca_value_targets", lib.rlca_value_targets(
@@ -154,7 +157,7 @@ def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_v
 
 
 def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
-                           gamma=0.99, out=None, time_major=False, multipass=False, workspace=None,
+                           gamma=0.99, out=None, time_major=False, multipass=False, inputs_ready=False, workspace=None,
                            stream=None):
     """Discounted returns G_t = r_t + gamma * G_{t+1} with the boundary rules."""
     lib = _lib.load()
@@ -166,7 +169,7 @@ def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_DISCOUNTED_RETURN, E, T, 0, flags, dev, workspace)
         check("rlca_discounted_return", lib.rlca_discounted_return(
@@ -176,7 +179,7 @@ def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value
 
 
 def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
-                   gamma=0.99, lambda_=0.95, out=None, time_major=False, multipass=False, workspace=None,
+                   gamma=0.99, lambda_=0.95, out=None, time_major=False, multipass=False, inputs_ready=False, workspace=None,
                    stream=None):
     """TD(lambda) returns."""
     lib = _lib.load()
@@ -189,7 +192,7 @@ def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_TD_LAMBDA, E, T, 0, flags, dev, workspace)
         check("rlca_td_lambda", lib.rlca_td_lambda(
@@ -200,7 +203,7 @@ def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value
 
 def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, truncated=None,
                 trunc_value=None, bootstrap=None, *, gamma=0.99, rho_bar=1.0, c_bar=1.0, lambda_=1.0,
-                vs=None, pg_advantages=None, want_pg=True, time_major=False, multipass=False,
+                vs=None, pg_advantages=None, want_pg=True, time_major=False, multipass=False, inputs_ready=False,
                 workspace=None, stream=None):
     """V-Trace targets and policy-gradient advantages: ``(vs, pg_advantages)``."""
     lib = _lib.load()
@@ -217,7 +220,7 @@ def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, t
         pg_advantages = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(vs, "vs", _F, shape, dev)
     _check(pg_advantages, "pg_advantages", _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VTRACE, E, T, 0, flags, dev, workspace)
         check("rlca_vtrace", lib.rlca_vtrace(
@@ -228,7 +231,7 @@ def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, t
 
 
 def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None, trunc_value=None,
-                 bootstrap=None, *, gamma=0.99, lambda_=0.95, out=None, time_major=False, multipass=False,
+                 bootstrap=None, *, gamma=0.99, lambda_=0.95, out=None, time_major=False, multipass=False, inputs_ready=False,
                  workspace=None, stream=None):
     """Retrace(lambda) Q targets; q and pi are [E, T, A] ([T, E, A])."""
     lib = _lib.load()
@@ -247,7 +250,7 @@ def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None,
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_RETRACE, E, T, A, flags, dev, workspace)
         check("rlca_retrace", lib.rlca_retrace(
@@ -258,7 +261,7 @@ def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None,
 
 
 def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0.95, out=None,
-                    time_major=False, multipass=False, workspace=None, stream=None):
+                    time_major=False, multipass=False, inputs_ready=False, workspace=None, stream=None):
     """Accumulating eligibility trace (forward scan)."""
     lib = _lib.load()
     dev = x.device
@@ -270,7 +273,7 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_ELIG_TRACE, E, T, 0, flags, dev, workspace)
         check("rlca_elig_trace", lib.rlca_elig_trace(
@@ -280,7 +283,7 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
 
 
 def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=False, flag_is_start=False,
-                             out=None, time_major=False, multipass=False, workspace=None, stream=None):
+                             out=None, time_major=False, multipass=False, inputs_ready=False, workspace=None, stream=None):
     """Per-episode running sum of x (int32 wraps; float32)."""
     lib = _lib.load()
     dev = x.device
@@ -299,7 +302,7 @@ def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=Fa
         out = torch.empty(shape, dtype=x.dtype, device=dev)
     _check(out, "out", (x.dtype,), shape, dev)
     extra = (_lib.RLCA_PSUM_EXCLUSIVE if exclusive else 0) | (_lib.RLCA_PSUM_FLAG_IS_START if flag_is_start else 0)
-    flags = _flags(time_major, multipass, extra)
+    flags = _flags(time_major, multipass, extra, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_PREFIX_SUM, E, T, 0, flags, dev, workspace)
         check("rlca_episodic_prefix_sum", lib.rlca_episodic_prefix_sum(
@@ -308,7 +311,7 @@ def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=Fa
     return out
 
 
-def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_major=False, multipass=False,
+def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_major=False, multipass=False, inputs_ready=False,
                      workspace=None, stream=None):
     """Generic A_t = alpha_t + beta_t * A_{t+1} (reverse) or A_{t-1} (forward)."""
     lib = _lib.load()
@@ -321,7 +324,7 @@ def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_ma
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=dev)
     _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_AFFINE_SCAN, E, T, 0, flags, dev, workspace)
         check("rlca_affine_scan", lib.rlca_affine_scan(

@@ -86,6 +86,15 @@ typedef struct CUstream_st *rlca_stream_t;
 /* Use the two-pass segmented path even where one pass would do (the library
  * picks it by itself for long rows on few environments).  Needs workspace. */
 #define RLCA_MULTIPASS           0x2u
+/* The caller asserts that this call's inputs were not written by the kernel
+ * that precedes it on the stream (they were complete before that kernel was
+ * enqueued).  The kernel may then read its inputs while the preceding kernel
+ * is still running, and only waits for it before writing anything, so
+ * back-to-back calls on independent batches overlap.  Without the flag a
+ * call reads nothing before the preceding kernel has completed.  Ignored by
+ * the two-pass path.  A false assertion gives wrong results (never an
+ * out-of-bounds access). */
+#define RLCA_INPUTS_READY        0x10u
 /* rlca_episodic_prefix_sum: output the sum over the steps BEFORE t in t's
  * episode instead of the inclusive sum. */
 #define RLCA_PSUM_EXCLUSIVE      0x4u

@@ -85,12 +85,12 @@ def make_inputs(kind, E, T, seed, trunc, device, **kw):
     raise ValueError(kind)
 
 
-def run_gpu(kind, d, time_major=False, multipass=False, params=None):
+def run_gpu(kind, d, time_major=False, multipass=False, params=None, inputs_ready=False):
     """Outputs of the CUDA path as env-major tensors (tuple)."""
     p = dict(gamma=GAMMA, lambda_=LAMBDA)
     p.update(params or {})
     x = _tm(d, time_major)
-    common = dict(time_major=time_major, multipass=multipass)
+    common = dict(time_major=time_major, multipass=multipass, inputs_ready=inputs_ready)
     if kind == "gae":
         out = rlca.rlca_gae(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
                             x["bootstrap"], gamma=p["gamma"], lambda_=p["lambda_"], **common)
@@ -168,11 +168,11 @@ def run_oracle(kind, d, rows, params=None):
 
 
 def check_case(kind, E, T, seed=0, trunc=True, time_major=False, multipass=False, params=None, device="cuda",
-               gen_device=None, rows=None, inputs=None, **gen_kw):
+               gen_device=None, rows=None, inputs=None, inputs_ready=False, **gen_kw):
     """Run one parity case; returns the worst relative error seen."""
     d = inputs if inputs is not None else make_inputs(kind, E, T, seed, trunc, gen_device or device, **gen_kw)
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    got = run_gpu(kind, d, time_major=time_major, multipass=multipass, params=params)
+    got = run_gpu(kind, d, time_major=time_major, multipass=multipass, params=params, inputs_ready=inputs_ready)
     torch.cuda.synchronize()
     if rows is None:
         rows = sample_rows(E, T, seed)

@@ -219,6 +219,48 @@ def test_deterministic_and_stream_ordered():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("kind", parity.KINDS)
+def test_inputs_ready_flag_gives_the_same_results(kind):
+    """RLCA_INPUTS_READY only changes when a kernel may start reading."""
+    for E, T, tm in ((4096, 128, False), (300, 1000, True), (7, 9000, False)):
+        parity.check_case(kind, E, T, seed=E + T, time_major=tm, inputs_ready=True)
+
+
+def test_inputs_ready_chain_keeps_stream_order():
+    """Back-to-back calls in one stream: calls flagged RLCA_INPUTS_READY
+    overlap their predecessor, while an unflagged call that reads the
+    previous call's output still sees it complete.  Each affine scan feeds
+    the next one's alpha; the final result must match running them one by
+    one with a synchronisation in between."""
+    E, T = 4096, 512
+    d = parity.make_inputs("affine_bwd", E, T, seed=91, trunc=False, device="cuda")
+    beta = d["beta"] * 0.5
+    indep = [torch.randn(E, T, device="cuda") for _ in range(6)]
+    torch.cuda.synchronize()
+    outs = []
+    cur = d["alpha"]
+    for i in range(6):
+        # unflagged: reads the previous result
+        cur = rlca.rlca_affine_scan(cur * 0 + cur, beta, None)  # copy kernel in between, then scan
+        cur = rlca.rlca_affine_scan(cur, beta, None)
+        # flagged calls on independent inputs interleaved
+        outs.append(rlca.rlca_affine_scan(indep[i], beta, None, inputs_ready=True))
+        cur = rlca.rlca_affine_scan(cur, beta, None)
+    torch.cuda.synchronize()
+    ref_cur = d["alpha"]
+    for i in range(6):
+        ref_cur = rlca.rlca_affine_scan(ref_cur * 0 + ref_cur, beta, None)
+        torch.cuda.synchronize()
+        ref_cur = rlca.rlca_affine_scan(ref_cur, beta, None)
+        torch.cuda.synchronize()
+        ref_i = rlca.rlca_affine_scan(indep[i], beta, None)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref_i)
+        ref_cur = rlca.rlca_affine_scan(ref_cur, beta, None)
+        torch.cuda.synchronize()
+    assert torch.equal(cur, ref_cur)
+
+
 def test_empty_inputs():
     z = torch.empty(0, 16, device="cuda")
     adv, ret = rlca.rlca_gae(z, z.clone())
