@@ -15,7 +15,8 @@ namespace {
 
 constexpr int64_t kMaxT = int64_t(1) << 30;
 constexpr int64_t kMaxE = INT32_MAX;
-constexpr size_t kMaxMapBytes = sizeof(Aff<F3>);  // largest affine map of any estimator
+constexpr size_t kMaxMapBytes = sizeof(Aff<F2>);  // largest affine map of any estimator
+
 
 int next_pow2(int64_t x) {
   int p = 1;
@@ -92,7 +93,7 @@ int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flag
   int sm = 0;
   if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
   Plan p;
-  if (!make_plan(kind, E, (int)T, A, flags, sm, &p)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(kind, E, (int)T, A, flags, sm, vec_ok && T % 4 == 0, &p)) return RLCA_ERR_INVALID_ARG;
   if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes || !aligned(ws, 16))) return RLCA_ERR_INVALID_ARG;
   Geom g;
   g.E = E;
@@ -108,11 +109,22 @@ int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flag
 
 }  // namespace
 
-bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, Plan* out) {
+bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec,
+               Plan* out) {
   const bool retrace = kind == Kind::Retrace;
   Plan q = {};
   q.time_major = (flags & RLCA_TIME_MAJOR) != 0;
-  if (q.time_major) {
+  q.staged = kStagedPath && vec && !q.time_major && !retrace && T % 4 == 0;
+  if (q.staged) {
+    int W = (int)std::min<int64_t>(next_pow2((T + kEsSteps - 1) / kEsSteps), kEsMaxWidth);
+    if (flags & RLCA_MULTIPASS) W = std::max(1, W / 4);
+    q.width = W;
+    q.block = std::max(W, kEsMinBlock);
+    q.rows_per_cta = q.block / W;
+    q.tile = kEsSteps * W;
+    q.smem_driver_bound = 0;  // sized by the launcher; at most ~90 KB
+    q.smem = 0;
+  } else if (q.time_major) {
     const int cmax = retrace ? kRetraceTmMaxWidth : kTmMaxWidth;
     int C = (int)std::min<int64_t>(next_pow2((T + 7) / 8), cmax);
     if (flags & RLCA_MULTIPASS) C = std::max(1, C / 4);
@@ -128,7 +140,7 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
                                    wmax);
     if (flags & RLCA_MULTIPASS) W = std::max(kEmMinWidth, W / 4);
     q.width = W;
-    q.block = std::max(W, 256);
+    q.block = std::max(W, kEmMinBlock);
     q.rows_per_cta = q.block / W;
     q.tile = kEmSteps * W;
     const int nwr = W > 32 ? W / 32 : 1;
@@ -152,9 +164,11 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const int seg_tiles = (q.ntiles + nseg - 1) / nseg;
   q.seg_len = seg_tiles * q.tile;
   q.nseg = (q.ntiles + seg_tiles - 1) / seg_tiles;
-  // one affine map per (row, segment): two values, three of each for the fused value targets
-  const size_t ws_elem = kind == Kind::ValueTargets ? 24 : 8;
+  // one affine map per (row, segment): two values, two of each for the fused value targets
+  const size_t ws_elem = kind == Kind::ValueTargets ? 16 : 8;
   q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
+  q.fast = !q.staged && !q.time_major && vec && T % kEmSteps == 0 && q.ntiles == 1 && q.nseg == 1 &&
+           !(flags & RLCA_MULTIPASS);
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
   *out = q;
@@ -204,9 +218,12 @@ int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions
   if (check_sizes(E, T, &st)) return st;
   int sm = 0;
   if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
-  Plan p;
-  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, &p)) return RLCA_ERR_INVALID_ARG;
-  *bytes = p.ws_bytes;
+  // the call picks the staged or the direct path from its pointers' alignment,
+  // which the query cannot see: report the larger of the two needs
+  Plan pd, ps;
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, false, &pd)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, true, &ps)) return RLCA_ERR_INVALID_ARG;
+  *bytes = std::max(pd.ws_bytes, ps.ws_bytes);
   return RLCA_OK;
 }
 
@@ -257,7 +274,7 @@ int rlca_value_targets(const float* rewards, const float* values, const uint8_t*
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
   auto fill = [&](auto& e) {
     e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.disc = disc_returns;
-    e.td = td_lambda_returns; e.gamma = gamma; e.gl = gamma * lambda; e.one_minus_lambda = 1.f - lambda;
+    e.td = td_lambda_returns; e.gamma = gamma; e.gl = gamma * lambda;
   };
   if (truncated) {
     ValueTargetsEst<true> e;

@@ -60,8 +60,58 @@ static cudaError_t launch_tm_c(const Plan& p, const Est& est, const Geom& g, cud
   }
 }
 
+template <class Est, int W>
+static cudaError_t launch_fast_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (W <= WidthCaps<Est>::em) {
+    using S = EmShape<W>;
+    const size_t drv = S::NWR > 1 ? (size_t)2 * S::ROWS * S::NWR * sizeof(Aff<typename Est::V>) : 0;
+    return launch_one<Est>(em_fast_kernel<Est, W>, p, drv + p.smem, est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est, int W>
+static cudaError_t launch_es_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (kStagedPath && Est::kStageable && W <= kEsMaxWidth) {
+    return launch_one<Est>(es_scan_kernel<Est, W>, p, es_smem_bytes<Est, W>(), est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
 template <class Est>
 static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if (p.fast) {
+    switch (p.width) {
+      case 1: return launch_fast_w<Est, 1>(p, est, g, s);
+      case 2: return launch_fast_w<Est, 2>(p, est, g, s);
+      case 4: return launch_fast_w<Est, 4>(p, est, g, s);
+      case 8: return launch_fast_w<Est, 8>(p, est, g, s);
+      case 16: return launch_fast_w<Est, 16>(p, est, g, s);
+      case 32: return launch_fast_w<Est, 32>(p, est, g, s);
+      case 64: return launch_fast_w<Est, 64>(p, est, g, s);
+      case 128: return launch_fast_w<Est, 128>(p, est, g, s);
+      case 256: return launch_fast_w<Est, 256>(p, est, g, s);
+      case 512: return launch_fast_w<Est, 512>(p, est, g, s);
+      case 1024: return launch_fast_w<Est, 1024>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  if (p.staged) {
+    switch (p.width) {
+      case 1: return launch_es_w<Est, 1>(p, est, g, s);
+      case 2: return launch_es_w<Est, 2>(p, est, g, s);
+      case 4: return launch_es_w<Est, 4>(p, est, g, s);
+      case 8: return launch_es_w<Est, 8>(p, est, g, s);
+      case 16: return launch_es_w<Est, 16>(p, est, g, s);
+      case 32: return launch_es_w<Est, 32>(p, est, g, s);
+      case 64: return launch_es_w<Est, 64>(p, est, g, s);
+      case 128: return launch_es_w<Est, 128>(p, est, g, s);
+      case 256: return launch_es_w<Est, 256>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
   if (p.time_major) {
     switch (p.width) {
       case 1: return launch_tm_c<Est, 1>(p, est, g, s);

@@ -17,18 +17,20 @@
 //   Regs<L>                     per-thread registers of L consecutive steps
 //   row_carry(row)              A_T (backward) / A_{-1} (forward) of a row
 //   stage / stage_tm            cooperative per-tile staging (Retrace only)
-//   load(...)                   read the thread's L steps
+//   load(R, io, ...)            read the thread's L steps through io (io.cuh)
 //   nb_give / nb_load / nb_take the neighbour step's inputs (step t0+L for a
 //                               backward scan, t0-1 for a forward one)
 //   coef(R, k, t)               (alpha_t, beta_t) of step t = t0 + k
 //   emit(R, k, A, adj, c)       output of step k from A_t (adj = A of the
 //                               step the recurrence reads)
-//   store(...)                  write the thread's outputs
+//   store(R, io)                write the thread's outputs through io
+//   kStageable, staged_io(f)    inputs / outputs the staged driver may stage
+//                               (floats, then flag bytes, then outputs)
 #pragma once
 
 #include <type_traits>
 
-#include "scan_core.cuh"
+#include "io.cuh"
 
 namespace rlca {
 
@@ -56,19 +58,25 @@ struct BoundaryRegs {
   float boot;            // bootstrap of the row when this thread holds step T-1
 };
 
-template <bool HAS_TRUNC, int L, class Lay>
-__device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryRegs<L>& R, const Lay& lay,
-                                              int64_t row, int t0, int n, bool vec) {
-  R.term = load_flags<L>(b.term, lay, row, t0, n, vec);
-  R.trunc = HAS_TRUNC ? (load_flags<L>(b.trunc, lay, row, t0, n, vec) & ~R.term) : 0u;
+// flags are staged byte inputs 0 (terminated) and 1 (truncated)
+template <bool HAS_TRUNC, int L, class IO>
+__device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryRegs<L>& R, const IO& io) {
+  R.term = io.template flags<L>(0, b.term);
+  R.trunc = HAS_TRUNC ? (io.template flags<L>(1, b.trunc) & ~R.term) : 0u;
 #pragma unroll
   for (int k = 0; k < L; ++k) R.tv[k] = 0.f;
   if (HAS_TRUNC && R.trunc != 0u) {  // truncations are rare: one branch instead of L predicated loads
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if ((R.trunc >> k) & 1u) R.tv[k] = __ldg(b.tv + lay.at(row, t0 + k));
+      if ((R.trunc >> k) & 1u) R.tv[k] = __ldg(b.tv + io.at(k));
   }
-  R.boot = (n > 0 && t0 + n == b.T && b.boot != nullptr) ? __ldg(b.boot + row) : 0.f;
+  R.boot = (io.n > 0 && io.t0 + io.n == b.T && b.boot != nullptr) ? __ldg(b.boot + io.row) : 0.f;
+}
+
+template <class F>
+__device__ __forceinline__ void staged_flags(const BoundaryArgs& b, F& f) {
+  f.in_b(b.term);
+  f.in_b(b.trunc);
 }
 
 // successor value of step k: 0 / trunc value / bootstrap / interior value
@@ -96,6 +104,16 @@ struct GaeEst : NoStage {
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 2, kSB = 2, kSO = 2;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(r);
+    f.in_f(v);
+    staged_flags(b, f);
+    f.out_f(adv);
+    f.out_f(ret);
+  }
   BoundaryArgs b;
   const float* r;
   const float* v;
@@ -110,12 +128,11 @@ struct GaeEst : NoStage {
     float oa[L], orr[L];
   };
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_vals<L>(v, lay, row, t0, n, vec, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, r, R.r);
+    io.template f<L>(1, v, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
@@ -138,11 +155,10 @@ struct GaeEst : NoStage {
     R.oa[k] = A;
     R.orr[k] = A + R.v[k];
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(adv, lay, row, t0, n, vec, R.oa);
-    if (ret != nullptr) store_vals<L>(ret, lay, row, t0, n, vec, R.orr);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, adv, R.oa);
+    io.template put<L>(1, ret, R.orr);
   }
 };
 
@@ -156,6 +172,14 @@ struct DiscEst : NoStage {
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(r);
+    staged_flags(b, f);
+    f.out_f(out);
+  }
   BoundaryArgs b;
   const float* r;
   float* out;
@@ -169,11 +193,10 @@ struct DiscEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t row) const {
     return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, r, R.r);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
@@ -191,10 +214,9 @@ struct DiscEst : NoStage {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
     R.o[k] = A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
   }
 };
 
@@ -208,6 +230,15 @@ struct TdLambdaEst : NoStage {
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 2, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(r);
+    f.in_f(v);
+    staged_flags(b, f);
+    f.out_f(out);
+  }
   BoundaryArgs b;
   const float* r;
   const float* v;
@@ -222,12 +253,11 @@ struct TdLambdaEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t row) const {
     return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_vals<L>(v, lay, row, t0, n, vec, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, r, R.r);
+    io.template f<L>(1, v, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
@@ -249,25 +279,40 @@ struct TdLambdaEst : NoStage {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
     R.o[k] = A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
   }
 };
 
 // ===========================================================================
 // Fused value targets: GAE (adv, ret), discounted return and TD(lambda) of
-// one rollout from a single read of r, V and the flags.  The three
-// recurrences are the ones of GaeEst, DiscEst and TdLambdaEst, scanned side
-// by side as one F3-valued affine map per step (.x GAE, .y discounted
-// return, .z TD(lambda)); carry A_T = (0, bootstrap, bootstrap).
+// one rollout from a single read of r, V and the flags.  GAE and the
+// discounted return are the recurrences of GaeEst and DiscEst, scanned side
+// by side as one F2-valued affine map per step (.x GAE, .y discounted
+// return; carry A_T = (0, bootstrap)).  The TD(lambda) return is written as
+// adv + V: the lambda-return satisfies G_t = A_t + V_t exactly under every
+// boundary rule (interior: r + gamma[(1-lambda)V_{t+1} + lambda G_{t+1}];
+// termination: r; truncation: r + gamma tv; window edge: r + gamma b), so
+// it needs no third scan.
 // ===========================================================================
 template <bool HAS_TRUNC>
 struct ValueTargetsEst : NoStage {
-  using V = F3;
+  using V = F2;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 2, kSB = 2, kSO = 4;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(r);
+    f.in_f(v);
+    staged_flags(b, f);
+    f.out_f(adv);
+    f.out_f(ret);
+    f.out_f(disc);
+    f.out_f(td);
+  }
   BoundaryArgs b;
   const float* r;
   const float* v;
@@ -275,24 +320,22 @@ struct ValueTargetsEst : NoStage {
   float* ret;
   float* disc;
   float* td;
-  float gamma, gl, one_minus_lambda;
+  float gamma, gl;
 
   template <int L>
   struct Regs {
     BoundaryRegs<L> bd;
     float r[L], v[L], vnext;
-    float oa[L], orr[L], od[L], ot[L];
+    float oa[L], od[L];
   };
-  __device__ __forceinline__ F3 row_carry(int64_t row) const {
-    const float bb = b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
-    return F3(0.f, bb, bb);
+  __device__ __forceinline__ F2 row_carry(int64_t row) const {
+    return F2(0.f, b.boot != nullptr ? __ldg(b.boot + row) : 0.f);
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_vals<L>(v, lay, row, t0, n, vec, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, r, R.r);
+    io.template f<L>(1, v, R.v);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
@@ -304,32 +347,28 @@ struct ValueTargetsEst : NoStage {
   template <int L>
   __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
   template <int L>
-  __device__ __forceinline__ Aff<F3> coef(const Regs<L>& R, int k, int t) const {
-    const bool tm = (R.bd.term >> k) & 1u, tr = (R.bd.trunc >> k) & 1u;
-    const bool last = t == b.T - 1;
-    const float v_in = (k + 1 < L) ? R.v[k + 1] : R.vnext;
-    const float vn = successor(R.bd, k, t, b.T, v_in);
+  __device__ __forceinline__ Aff<F2> coef(const Regs<L>& R, int k, int t) const {
+    const bool tr = (R.bd.trunc >> k) & 1u;
+    const bool c = cut(R.bd, k);
+    const float vn = successor(R.bd, k, t, b.T, (k + 1 < L) ? R.v[k + 1] : R.vnext);
     const float delta = R.r[k] + gamma * vn - R.v[k];
     const float a_disc = tr ? R.r[k] + gamma * R.bd.tv[k] : R.r[k];
-    const float tail = tm ? 0.f : (tr ? R.bd.tv[k] : one_minus_lambda * (last ? R.bd.boot : v_in));
-    const float a_td = R.r[k] + gamma * tail;
-    const bool c = tm || tr;
-    return {F3(delta, a_disc, a_td), F3((c || last) ? 0.f : gl, c ? 0.f : gamma, c ? 0.f : gl)};
+    return {F2(delta, a_disc), F2((c || t == b.T - 1) ? 0.f : gl, c ? 0.f : gamma)};
   }
   template <int L>
-  __device__ __forceinline__ void emit(Regs<L>& R, int k, F3 A, F3, const Aff<F3>&) const {
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, F2 A, F2, const Aff<F2>&) const {
     R.oa[k] = A.x;
-    R.orr[k] = A.x + R.v[k];
     R.od[k] = A.y;
-    R.ot[k] = A.z;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    if (adv != nullptr) store_vals<L>(adv, lay, row, t0, n, vec, R.oa);
-    if (ret != nullptr) store_vals<L>(ret, lay, row, t0, n, vec, R.orr);
-    if (disc != nullptr) store_vals<L>(disc, lay, row, t0, n, vec, R.od);
-    if (td != nullptr) store_vals<L>(td, lay, row, t0, n, vec, R.ot);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    float ret_[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) ret_[k] = R.oa[k] + R.v[k];
+    io.template put<L>(0, adv, R.oa);
+    io.template put<L>(1, ret, ret_);
+    io.template put<L>(2, disc, R.od);
+    io.template put<L>(3, td, ret_);
   }
 };
 
@@ -345,6 +384,18 @@ struct VtraceEst : NoStage {
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 4, kSB = 2, kSO = 2;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(r);
+    f.in_f(v);
+    f.in_f(lpt);
+    f.in_f(lpb);
+    staged_flags(b, f);
+    f.out_f(vs);
+    f.out_f(pg);
+  }
   BoundaryArgs b;
   const float* r;
   const float* v;
@@ -362,15 +413,14 @@ struct VtraceEst : NoStage {
     int t0;
   };
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     float a[L], bb[L];
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_vals<L>(v, lay, row, t0, n, vec, R.v);
-    load_vals<L>(lpt, lay, row, t0, n, vec, a);
-    load_vals<L>(lpb, lay, row, t0, n, vec, bb);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
+    io.template f<L>(0, r, R.r);
+    io.template f<L>(1, v, R.v);
+    io.template f<L>(2, lpt, a);
+    io.template f<L>(3, lpb, bb);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
 #pragma unroll
     for (int k = 0; k < L; ++k) {
       const float ratio = expf(a[k] - bb[k]);
@@ -378,7 +428,7 @@ struct VtraceEst : NoStage {
       R.c[k] = lambda * fminf(c_bar, ratio);
     }
     R.vnext = 0.f;
-    R.t0 = t0;
+    R.t0 = io.t0;
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
@@ -402,11 +452,10 @@ struct VtraceEst : NoStage {
     const float nvs = successor(R.bd, k, R.t0 + k, b.T, vn + adj);
     R.opg[k] = R.rho[k] * (R.r[k] + gamma * nvs - R.v[k]);
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(vs, lay, row, t0, n, vec, R.ovs);
-    if (pg != nullptr) store_vals<L>(pg, lay, row, t0, n, vec, R.opg);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, vs, R.ovs);
+    io.template put<L>(1, pg, R.opg);
   }
 };
 
@@ -464,6 +513,8 @@ struct RetraceEst {
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
+  static constexpr bool kStageable = false;
+  static constexpr int kSF = 0, kSB = 0, kSO = 0;  // staged float inputs, flag inputs, outputs
   BoundaryArgs b;
   RetraceStage st;
   const float* r;
@@ -522,12 +573,13 @@ struct RetraceEst {
     __syncthreads();
   }
 
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int slot, int t0, int n,
-                                       bool vec, int ts, int tile, int nrows, unsigned char* sm) const {
-    load_vals<L>(r, lay, row, t0, n, vec, R.r);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, lay, row, t0, n, vec);
-    constexpr bool kTM = Lay::kTimeMajor;
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int slot, int ts, int tile, int nrows,
+                                       unsigned char* sm) const {
+    io.template f<L>(0, r, R.r);
+    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    constexpr bool kTM = IO::kTimeMajor;
+    const int t0 = io.t0, n = io.n;
     const int NW = blockDim.x >> 5;
     const float* s_ev = reinterpret_cast<const float*>(sm) + NW * 64 * st.A;
     const int srows = tile + 1;
@@ -569,10 +621,9 @@ struct RetraceEst {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
     R.o[k] = A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
   }
 };
 
@@ -584,6 +635,15 @@ struct EligEst : NoStage {
   using V = float;
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(x);
+    f.in_b(term);
+    f.in_b(trunc);
+    f.out_f(out);
+  }
   const float* x;
   const uint8_t* term;   // nullable
   const uint8_t* trunc;  // nullable
@@ -597,11 +657,10 @@ struct EligEst : NoStage {
     float prev_done;
   };
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(x, lay, row, t0, n, vec, R.x);
-    R.done = load_flags<L>(term, lay, row, t0, n, vec) | load_flags<L>(trunc, lay, row, t0, n, vec);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, x, R.x);
+    R.done = io.template flags<L>(0, term) | io.template flags<L>(1, trunc);
     R.prev_done = 1.f;
   }
   template <int L>
@@ -623,10 +682,9 @@ struct EligEst : NoStage {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
     R.o[k] = A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
   }
 };
 
@@ -643,6 +701,15 @@ struct PrefixSumEst : NoStage {
   using V = VT;
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(x);
+    f.in_b(term);
+    f.in_b(trunc);
+    f.out_f(out);
+  }
   const void* x;
   const uint8_t* term;
   const uint8_t* trunc;
@@ -657,15 +724,14 @@ struct PrefixSumEst : NoStage {
     float prev_done;
   };
   __device__ __forceinline__ V row_carry(int64_t) const { return V(0); }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     if constexpr (std::is_integral<V>::value) {
-      load_ints<L>(static_cast<const int32_t*>(x), lay, row, t0, n, vec, R.x);
+      io.template i<L>(0, static_cast<const int32_t*>(x), R.x);
     } else {
-      load_vals<L>(static_cast<const float*>(x), lay, row, t0, n, vec, R.x);
+      io.template f<L>(0, static_cast<const float*>(x), R.x);
     }
-    R.done = load_flags<L>(term, lay, row, t0, n, vec) | load_flags<L>(trunc, lay, row, t0, n, vec);
+    R.done = io.template flags<L>(0, term) | io.template flags<L>(1, trunc);
     R.prev_done = 1.f;
   }
   template <int L>
@@ -691,13 +757,12 @@ struct PrefixSumEst : NoStage {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, V A, V adj, const Aff<V>& c) const {
     R.o[k] = exclusive ? (c.b != V(0) ? adj : V(0)) : A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
     if constexpr (std::is_integral<V>::value) {
-      store_ints<L>(static_cast<int32_t*>(out), lay, row, t0, n, vec, R.o);
+      io.template put_i<L>(0, static_cast<int32_t*>(out), R.o);
     } else {
-      store_vals<L>(static_cast<float*>(out), lay, row, t0, n, vec, R.o);
+      io.template put<L>(0, static_cast<float*>(out), R.o);
     }
   }
 };
@@ -710,6 +775,14 @@ struct AffineEst : NoStage {
   using V = float;
   static constexpr bool kBackward = BWD;
   static constexpr int kNb = 0;
+  static constexpr bool kStageable = true;
+  static constexpr int kSF = 2, kSB = 0, kSO = 1;  // staged float inputs, flag inputs, outputs
+  template <class F>
+  __device__ __forceinline__ void staged_io(F& f) const {
+    f.in_f(alpha);
+    f.in_f(beta);
+    f.out_f(out);
+  }
   const float* alpha;
   const float* beta;
   const float* carry;  // [E], nullable
@@ -722,11 +795,10 @@ struct AffineEst : NoStage {
   __device__ __forceinline__ float row_carry(int64_t row) const {
     return carry != nullptr ? __ldg(carry + row) : 0.f;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void load(Regs<L>& R, const Lay& lay, int64_t row, int, int t0, int n, bool vec,
-                                       int, int, int, unsigned char*) const {
-    load_vals<L>(alpha, lay, row, t0, n, vec, R.a);
-    load_vals<L>(beta, lay, row, t0, n, vec, R.b);
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, alpha, R.a);
+    io.template f<L>(1, beta, R.b);
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
@@ -742,10 +814,9 @@ struct AffineEst : NoStage {
   __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
     R.o[k] = A;
   }
-  template <int L, class Lay>
-  __device__ __forceinline__ void store(const Regs<L>& R, const Lay& lay, int64_t row, int t0, int n,
-                                        bool vec) const {
-    store_vals<L>(out, lay, row, t0, n, vec, R.o);
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
   }
 };
 

@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "estimators.cuh"
+#include "drivers.cuh"
 
 namespace rlca {
 
@@ -23,6 +23,8 @@ constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 struct Plan {
   bool time_major;
+  bool staged;      // env-major tiles staged through shared memory (es_scan_kernel)
+  bool fast;        // env-major, one tile per row, one segment (em_fast_kernel)
   int width;        // env-major: threads per row; time-major: chunk-threads per environment
   int block;        // threads per CTA
   int rows_per_cta;
@@ -37,7 +39,16 @@ struct Plan {
 };
 
 // Fills *p for a problem; returns false when the sizes cannot be launched.
-bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, Plan* p);
+// vec: the env-major arrays are 16-byte aligned (4-byte for flags) and
+// T % 4 == 0, so rows can be read as 16-byte vectors.
+bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec, Plan* p);
+
+#ifndef RLCA_STAGED_PATH
+#define RLCA_STAGED_PATH 0
+#endif
+// build-time choice: env-major tiles staged through shared memory
+// (es_scan_kernel) instead of the register drivers
+constexpr bool kStagedPath = RLCA_STAGED_PATH != 0;
 
 // Launches the scan of one estimator functor (both passes of the two-pass
 // path when p.nseg > 1).  Defined by explicit instantiation in the family

@@ -47,34 +47,34 @@ __device__ __forceinline__ Aff<V> compose(const Aff<V>& outer, const Aff<V>& inn
   return {outer.a + outer.b * inner.a, outer.b * inner.b};
 }
 
-// Three independent recurrences scanned side by side (the fused value-target
-// scan: GAE, discounted return and TD(lambda) of one row).  Arithmetic is
-// element-wise, so compose() on Aff<F3> composes the three maps at once.
-struct F3 {
-  float x, y, z;
-  __host__ __device__ F3() = default;
-  __host__ __device__ constexpr F3(float s) : x(s), y(s), z(s) {}
-  __host__ __device__ constexpr F3(float a, float b, float c) : x(a), y(b), z(c) {}
+// Two independent recurrences scanned side by side (the fused value-target
+// scan: GAE and the discounted return of one row).  Arithmetic is
+// element-wise, so compose() on Aff<F2> composes both maps at once.
+struct F2 {
+  float x, y;
+  F2() = default;
+  __host__ __device__ constexpr F2(float s) : x(s), y(s) {}
+  __host__ __device__ constexpr F2(float a, float b) : x(a), y(b) {}
 };
-__device__ __forceinline__ F3 operator+(const F3& a, const F3& b) { return {a.x + b.x, a.y + b.y, a.z + b.z}; }
-__device__ __forceinline__ F3 operator*(const F3& a, const F3& b) { return {a.x * b.x, a.y * b.y, a.z * b.z}; }
+__device__ __forceinline__ F2 operator+(const F2& a, const F2& b) { return {a.x + b.x, a.y + b.y}; }
+__device__ __forceinline__ F2 operator*(const F2& a, const F2& b) { return {a.x * b.x, a.y * b.y}; }
 
 __device__ __forceinline__ float shfl_down_v(float v, int d, int w) { return __shfl_down_sync(kFullMask, v, d, w); }
 __device__ __forceinline__ uint32_t shfl_down_v(uint32_t v, int d, int w) {
   return __shfl_down_sync(kFullMask, v, d, w);
 }
-__device__ __forceinline__ F3 shfl_down_v(const F3& v, int d, int w) {
-  return {shfl_down_v(v.x, d, w), shfl_down_v(v.y, d, w), shfl_down_v(v.z, d, w)};
+__device__ __forceinline__ F2 shfl_down_v(const F2& v, int d, int w) {
+  return {shfl_down_v(v.x, d, w), shfl_down_v(v.y, d, w)};
 }
 __device__ __forceinline__ float shfl_up_v(float v, int d, int w) { return __shfl_up_sync(kFullMask, v, d, w); }
 __device__ __forceinline__ uint32_t shfl_up_v(uint32_t v, int d, int w) { return __shfl_up_sync(kFullMask, v, d, w); }
-__device__ __forceinline__ F3 shfl_up_v(const F3& v, int d, int w) {
-  return {shfl_up_v(v.x, d, w), shfl_up_v(v.y, d, w), shfl_up_v(v.z, d, w)};
+__device__ __forceinline__ F2 shfl_up_v(const F2& v, int d, int w) {
+  return {shfl_up_v(v.x, d, w), shfl_up_v(v.y, d, w)};
 }
 __device__ __forceinline__ float shfl_idx_v(float v, int s, int w) { return __shfl_sync(kFullMask, v, s, w); }
 __device__ __forceinline__ uint32_t shfl_idx_v(uint32_t v, int s, int w) { return __shfl_sync(kFullMask, v, s, w); }
-__device__ __forceinline__ F3 shfl_idx_v(const F3& v, int s, int w) {
-  return {shfl_idx_v(v.x, s, w), shfl_idx_v(v.y, s, w), shfl_idx_v(v.z, s, w)};
+__device__ __forceinline__ F2 shfl_idx_v(const F2& v, int s, int w) {
+  return {shfl_idx_v(v.x, s, w), shfl_idx_v(v.y, s, w)};
 }
 
 template <class V>
@@ -247,16 +247,64 @@ struct Geom {
 #endif
 constexpr int kEmSteps = RLCA_EM_STEPS;
 
-// env-major: TPR threads per row, kEmSteps steps per thread, rows packed 256 threads per CTA
+// smallest env-major CTA (rows shorter than this share a CTA)
+#ifndef RLCA_EM_MIN_BLOCK
+#define RLCA_EM_MIN_BLOCK 128
+#endif
+constexpr int kEmMinBlock = RLCA_EM_MIN_BLOCK;
+
+// env-major: TPR threads per row, kEmSteps steps per thread, rows packed kEmMinBlock threads per CTA
 template <int TPR>
 struct EmShape {
   static constexpr int L = kEmSteps;
   static constexpr int TILE = TPR * L;
-  static constexpr int BLOCK = TPR >= 256 ? TPR : 256;
+  static constexpr int BLOCK = TPR >= kEmMinBlock ? TPR : kEmMinBlock;
   static constexpr int ROWS = BLOCK / TPR;
   static constexpr int GW = TPR < 32 ? TPR : 32;       // lanes of one row inside a warp
   static constexpr int NWR = TPR > 32 ? TPR / 32 : 1;  // warps per row
 };
+
+// staged env-major (shared-memory tiles): TPR threads per row, SL steps per
+// thread, rows packed kEsMinBlock threads per CTA
+#ifndef RLCA_ES_STEPS
+#define RLCA_ES_STEPS 16
+#endif
+#ifndef RLCA_ES_MIN_BLOCK
+#define RLCA_ES_MIN_BLOCK 128
+#endif
+constexpr int kEsSteps = RLCA_ES_STEPS;
+constexpr int kEsMinBlock = RLCA_ES_MIN_BLOCK;
+constexpr int kEsMaxWidth = 256;
+
+template <int TPR>
+struct EsShape {
+  static constexpr int L = kEsSteps;
+  static constexpr int TILE = TPR * L;
+  static constexpr int BLOCK = TPR >= kEsMinBlock ? TPR : kEsMinBlock;
+  static constexpr int ROWS = BLOCK / TPR;
+  static constexpr int GW = TPR < 32 ? TPR : 32;
+  static constexpr int NWR = TPR > 32 ? TPR / 32 : 1;
+  static constexpr int PAD = L + 4;            // floats per thread slot in a float buffer
+  static constexpr int FSTRIDE = BLOCK * PAD;  // floats per float buffer
+  static constexpr int BSTRIDE = BLOCK * L;    // bytes per flag buffer
+  static constexpr int CHUNKS = ROWS * TILE / 4;  // 4-element chunks per CTA tile
+};
+
+__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// async global -> shared copies (completed by cp_async_wait_all, a hardware
+// wait on the thread's own copies)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
 
 // time-major: 32 environments per warp, C chunk-threads per environment, L steps each
 template <int C>
@@ -280,267 +328,6 @@ __device__ __forceinline__ V segment_carry_in(const Geom& g, int64_t row, int se
     for (int s = 0; s < seg; ++s) c = ws[s].a + ws[s].b * c;
   }
   return c;
-}
-
-// ---------------------------------------------------------------------------
-// env-major driver
-// ---------------------------------------------------------------------------
-template <class Est, int TPR>
-__global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
-    em_scan_kernel(Est est, Geom g) {
-  using S = EmShape<TPR>;
-  using V = typename Est::V;
-  constexpr bool BWD = Est::kBackward;
-  constexpr int L = S::L, GW = S::GW, NWR = S::NWR;
-
-  extern __shared__ __align__(16) unsigned char smem[];
-  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);  // [2][ROWS][NWR] warp totals (NWR > 1)
-  unsigned char* est_smem = smem + (NWR > 1 ? 2 * S::ROWS * NWR * sizeof(Aff<V>) : 0);
-
-  const int tid = threadIdx.x;
-  const int j = tid % TPR;
-  const int rloc = tid / TPR;
-  const int lane = tid & 31;
-  const int lig = j % GW;
-  const int wr = j / 32;
-  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
-  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * S::ROWS;
-  const int64_t row = row0 + rloc;
-  const bool row_ok = row < g.E;
-  const int seg_lo = seg * g.seg_len;
-  const int seg_hi = min(g.T, seg_lo + g.seg_len);
-  const bool vec = g.vec != 0;
-  const bool agg_mode = g.mode == kModeAggregate;
-  const EnvMajor lay{g.E, g.T};
-  const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
-  if (!early) pdl_wait();
-
-  Aff<V> carry;
-  if (agg_mode) {
-    carry = aff_identity<V>();
-  } else {
-    V c0 = row_ok ? est.row_carry(row) : V(0);
-    if (g.nseg > 1 && row_ok) c0 = segment_carry_in<V, BWD>(g, row, seg, c0);
-    carry = {c0, V(0)};
-  }
-
-  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
-  for (int it = 0; it < ntiles; ++it) {
-    const int tile = BWD ? ntiles - 1 - it : it;
-    const int ts = seg_lo + tile * S::TILE;
-    const int te = min(seg_hi, ts + S::TILE);
-    const int t0 = ts + j * L;
-    const int n = row_ok ? max(0, min(L, te - t0)) : 0;
-
-    est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, ts, te, est_smem);
-    typename Est::template Regs<L> R;
-    est.template load<L>(R, lay, row, rloc, t0, n, vec, ts, S::TILE, S::ROWS, est_smem);
-    if (it == ntiles - 1) pdl_trigger();
-
-    if constexpr (Est::kNb > 0) {
-      // neighbour step's inputs: from the adjacent lane when it holds them,
-      // else straight from memory
-      float give[Est::kNb > 0 ? Est::kNb : 1], got[Est::kNb > 0 ? Est::kNb : 1];
-      est.nb_give(R, give);
-#pragma unroll
-      for (int i = 0; i < Est::kNb; ++i)
-        got[i] = BWD ? __shfl_down_sync(kFullMask, give[i], 1, GW) : __shfl_up_sync(kFullMask, give[i], 1, GW);
-      const int tn = BWD ? t0 + L : t0 - 1;
-      const bool edge = BWD ? (lig == GW - 1 || t0 + L >= te) : (lig == 0);
-      if (n > 0 && edge && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
-      est.nb_take(R, got);
-    }
-
-    Aff<V> c[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) c[k] = (k < n) ? est.coef(R, k, t0 + k) : aff_identity<V>();
-    Aff<V> agg = aff_identity<V>();
-    if (BWD) {
-#pragma unroll
-      for (int k = L - 1; k >= 0; --k) agg = compose(c[k], agg);
-    } else {
-#pragma unroll
-      for (int k = 0; k < L; ++k) agg = compose(c[k], agg);
-    }
-
-    // inclusive scan of the thread maps inside the row's lane group
-    Aff<V> inc = agg;
-#pragma unroll
-    for (int off = 1; off < GW; off <<= 1) {
-      if (BWD) {
-        Aff<V> o = shfl_down_aff(inc, off, GW);
-        if (lig + off < GW) inc = compose(inc, o);
-      } else {
-        Aff<V> o = shfl_up_aff(inc, off, GW);
-        if (lig >= off) inc = compose(inc, o);
-      }
-    }
-    Aff<V> exc = BWD ? shfl_down_aff(inc, 1, GW) : shfl_up_aff(inc, 1, GW);
-    if (lig == (BWD ? GW - 1 : 0)) exc = aff_identity<V>();
-
-    Aff<V> boundary, next_carry;
-    if constexpr (NWR > 1) {
-      Aff<V>* x = xw + ((it & 1) * S::ROWS + rloc) * NWR;
-      if (lane == (BWD ? 0 : 31)) x[wr] = inc;
-      __syncthreads();
-      Aff<V> cc = carry;
-      boundary = cc;
-      if (BWD) {
-#pragma unroll 4
-        for (int w = NWR - 1; w >= 0; --w) {
-          if (w == wr) boundary = cc;
-          cc = compose(x[w], cc);
-        }
-      } else {
-#pragma unroll 4
-        for (int w = 0; w < NWR; ++w) {
-          if (w == wr) boundary = cc;
-          cc = compose(x[w], cc);
-        }
-      }
-      next_carry = cc;
-    } else {
-      boundary = carry;
-      Aff<V> tot = shfl_idx_aff(inc, BWD ? 0 : GW - 1, GW);
-      next_carry = compose(tot, carry);
-    }
-
-    if (!agg_mode) {
-      V A = compose(exc, boundary).a;  // value just outside this thread's chunk
-      if (BWD) {
-#pragma unroll
-        for (int k = L - 1; k >= 0; --k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      }
-      if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
-      est.template store<L>(R, lay, row, t0, n, vec);
-    }
-    carry = next_carry;
-  }
-  if (agg_mode && row_ok && j == 0) reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
-}
-
-// ---------------------------------------------------------------------------
-// time-major driver
-// ---------------------------------------------------------------------------
-template <class Est, int C>
-__global__ void __launch_bounds__(TmShape<C>::BLOCK)
-    tm_scan_kernel(Est est, Geom g) {
-  using S = TmShape<C>;
-  using V = typename Est::V;
-  constexpr bool BWD = Est::kBackward;
-  constexpr int L = S::L;
-
-  extern __shared__ __align__(16) unsigned char smem[];
-  Aff<V>* xs = reinterpret_cast<Aff<V>*>(smem);  // [2][C][32] chunk maps
-  unsigned char* est_smem = smem + 2 * C * 32 * sizeof(Aff<V>);
-
-  const int lane = threadIdx.x & 31;
-  const int cw = threadIdx.x >> 5;  // chunk index inside the tile
-  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
-  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * S::EW;
-  const int64_t row = row0 + lane;
-  const bool row_ok = row < g.E;
-  const int seg_lo = seg * g.seg_len;
-  const int seg_hi = min(g.T, seg_lo + g.seg_len);
-  const bool agg_mode = g.mode == kModeAggregate;
-  const TimeMajor lay{g.E, g.T};
-  const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
-  if (!early) pdl_wait();
-
-  Aff<V> carry;
-  if (agg_mode) {
-    carry = aff_identity<V>();
-  } else {
-    V c0 = row_ok ? est.row_carry(row) : V(0);
-    if (g.nseg > 1 && row_ok) c0 = segment_carry_in<V, BWD>(g, row, seg, c0);
-    carry = {c0, V(0)};
-  }
-
-  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
-  for (int it = 0; it < ntiles; ++it) {
-    const int tile = BWD ? ntiles - 1 - it : it;
-    const int ts = seg_lo + tile * S::TILE;
-    const int te = min(seg_hi, ts + S::TILE);
-    const int t0 = ts + cw * L;
-    const int n = row_ok ? max(0, min(L, te - t0)) : 0;
-
-    est.template stage_tm<S::BLOCK>(lay, row0, ts, te, est_smem);
-    typename Est::template Regs<L> R;
-    est.template load<L>(R, lay, row, lane, t0, n, false, ts, S::TILE, 32, est_smem);
-    if (it == ntiles - 1) pdl_trigger();
-    if constexpr (Est::kNb > 0) {
-      float got[Est::kNb > 0 ? Est::kNb : 1];
-#pragma unroll
-      for (int i = 0; i < Est::kNb; ++i) got[i] = 0.f;
-      const int tn = BWD ? t0 + L : t0 - 1;
-      if (n > 0 && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
-      est.nb_take(R, got);
-    }
-
-    Aff<V> c[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) c[k] = (k < n) ? est.coef(R, k, t0 + k) : aff_identity<V>();
-    Aff<V> agg = aff_identity<V>();
-    if (BWD) {
-#pragma unroll
-      for (int k = L - 1; k >= 0; --k) agg = compose(c[k], agg);
-    } else {
-#pragma unroll
-      for (int k = 0; k < L; ++k) agg = compose(c[k], agg);
-    }
-
-    Aff<V>* x = xs + (it & 1) * C * 32;
-    x[cw * 32 + lane] = agg;
-    __syncthreads();
-    Aff<V> cc = carry, boundary = carry;
-    if (BWD) {
-#pragma unroll 4
-      for (int w = C - 1; w >= 0; --w) {
-        if (w == cw) boundary = cc;
-        cc = compose(x[w * 32 + lane], cc);
-      }
-    } else {
-#pragma unroll 4
-      for (int w = 0; w < C; ++w) {
-        if (w == cw) boundary = cc;
-        cc = compose(x[w * 32 + lane], cc);
-      }
-    }
-
-    if (!agg_mode) {
-      V A = boundary.a;
-      if (BWD) {
-#pragma unroll
-        for (int k = L - 1; k >= 0; --k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      }
-      if (early && it == 0) pdl_wait();
-      est.template store<L>(R, lay, row, t0, n, false);
-    }
-    carry = cc;
-  }
-  if (agg_mode && row_ok && cw == 0) reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
 }
 
 }  // namespace rlca

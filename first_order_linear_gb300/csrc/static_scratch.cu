@@ -77,14 +77,14 @@ extern "C" int rlca_gae_static_scratch(const float* rewards, const float* values
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RLCA_ERR_CUDA;
   int sms = 0;
   if (sm_count(dev, &sms) != cudaSuccess) return RLCA_ERR_CUDA;
+  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) && aligned(returns, 16) &&
+                   aligned(terminated, 4) && aligned(truncated, 4);
   Plan p;
-  if (!make_plan(Kind::Gae, E, (int)T, 0, flags, sms, &p)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(Kind::Gae, E, (int)T, 0, flags, sms, vec && T % 4 == 0, &p)) return RLCA_ERR_INVALID_ARG;
   if (p.ws_bytes > RLCA_STATIC_SCRATCH_BYTES) return RLCA_ERR_UNSUPPORTED;
   void* ws = nullptr;
   if (p.ws_bytes > 0 && scratch_address(dev, &ws) != cudaSuccess) return RLCA_ERR_CUDA;
 
-  const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) && aligned(returns, 16) &&
-                   aligned(terminated, 4) && aligned(truncated, 4);
   Geom g;
   g.E = E;
   g.T = (int)T;

@@ -165,16 +165,17 @@ int rlca_gae(const float *rewards, const float *values,
 /*
  * Fused value targets: GAE advantages and returns, discounted returns and
  * TD(lambda) returns of the same rollout in one pass that reads rewards,
- * values and flags once (the three recurrences of rlca_gae,
- * rlca_discounted_return and rlca_td_lambda, scanned side by side; rl-triton
- * §4 Fusion: constructing coefficients on chip removes intermediate HBM
- * round trips).  Results equal those of the three separate calls (the
- * floating-point grouping may differ within rounding).
+ * values and flags once (rl-triton §4 Fusion: constructing coefficients on
+ * chip removes intermediate HBM round trips).  The recurrences of rlca_gae
+ * and rlca_discounted_return are scanned side by side; the TD(lambda) return
+ * is written as advantages + values, which equals it exactly under every
+ * boundary rule, so it needs no third scan.  Results equal those of the
+ * separate calls within floating-point rounding.
  *   rewards, values, terminated, truncated, trunc_value, bootstrap  as rlca_gae
  *   advantages, returns        [E,T] f32 outputs of rlca_gae, each nullable
  *   disc_returns               [E,T] f32 output of rlca_discounted_return, nullable
  *   td_lambda_returns          [E,T] f32 output of rlca_td_lambda, nullable
- * At least one output must be given.  Workspace (two-pass path): 24 bytes
+ * At least one output must be given.  Workspace (two-pass path): 16 bytes
  * per row per segment (rlca_workspace_size with RLCA_EST_VALUE_TARGETS).
  */
 int rlca_value_targets(const float *rewards, const float *values,
