@@ -453,6 +453,119 @@ def run_e2e(args, d_cpu, dev):
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
 
 
+# --------------------------------------------------------------------------
+# --sweep: device throughput of every estimator on the benchmark shapes
+# --------------------------------------------------------------------------
+
+SWEEP_KINDS = ("gae", "disc", "td", "vt", "vtrace", "retrace", "elig", "psum")
+
+
+def _sweep_case(kind, E, T, trunc, dev):
+    """Seeded inputs (env-major), the algorithmic bytes of one call, and the
+    output buffers' shapes and dtypes."""
+    import torch
+    from first_order_linear_gb300 import synth
+    seed = synth.config_seed(f"bench-{kind}-{E}-{T}-{trunc}")
+    A = synth.NUM_ACTIONS
+    f32 = torch.float32
+    if kind in ("gae", "disc", "td", "vt"):
+        d = synth.value_rollout(E, T, seed, p_term=P_TERM, p_trunc=P_TRUNC, with_trunc=trunc, device=dev)
+        reads = {"gae": 9, "disc": 5, "td": 9, "vt": 9}[kind]
+        outs = {"gae": 2, "disc": 1, "td": 1, "vt": 4}[kind]
+        spec = [((E, T), f32)] * outs
+    elif kind == "vtrace":
+        d = synth.vtrace_rollout(E, T, seed, p_term=0.01, p_trunc=P_TRUNC if trunc else 0.0, with_trunc=trunc,
+                                 device=dev)
+        reads, spec = 17, [((E, T), f32)] * 2
+    elif kind == "retrace":
+        d = synth.retrace_rollout(E, T, seed, p_term=0.002, p_trunc=P_TRUNC if trunc else 0.0, with_trunc=trunc,
+                                  device=dev)
+        reads, spec = 8 * A + 13, [((E, T), f32)]
+    else:
+        d = synth.forward_rollout(E, T, seed, p_term=0.01, p_trunc=P_TRUNC, with_trunc=trunc, device=dev)
+        reads, spec = 5, [((E, T), f32 if kind == "elig" else torch.int32)]
+    n_trunc = int(d["truncated"].sum()) if d.get("truncated") is not None else 0
+    per_step = reads + (1 if d.get("truncated") is not None else 0) + 4 * len(spec)
+    tv_bytes = 32 * n_trunc if kind in ("gae", "disc", "td", "vt", "vtrace", "retrace") else 0
+    return d, per_step * E * T + tv_bytes, spec
+
+
+def _sweep_call(kind, x, o, tm):
+    from first_order_linear_gb300 import rlca
+    kw = dict(time_major=tm)
+    b = (x.get("terminated"), x.get("truncated"), x.get("trunc_value"), x.get("bootstrap"))
+    if kind == "gae":
+        rlca.rlca_gae(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, advantages=o[0], returns=o[1], **kw)
+    elif kind == "disc":
+        rlca.rlca_discounted_return(x["rewards"], *b, gamma=GAMMA, out=o[0], **kw)
+    elif kind == "td":
+        rlca.rlca_td_lambda(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, out=o[0], **kw)
+    elif kind == "vt":
+        rlca.rlca_value_targets(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, advantages=o[0],
+                                returns=o[1], disc_returns=o[2], td_lambda_returns=o[3], **kw)
+    elif kind == "vtrace":
+        rlca.rlca_vtrace(x["rewards"], x["values"], x["logp_target"], x["logp_behaviour"], *b, gamma=GAMMA, vs=o[0],
+                         pg_advantages=o[1], **kw)
+    elif kind == "retrace":
+        rlca.rlca_retrace(x["q"], x["pi"], x["mu_a"], x["actions"], x["rewards"], *b, gamma=GAMMA, lambda_=LAMBDA,
+                          out=o[0], **kw)
+    elif kind == "elig":
+        rlca.rlca_elig_trace(x["x_f32"], x["terminated"], x["truncated"], gamma=GAMMA, lambda_=LAMBDA, out=o[0], **kw)
+    else:
+        rlca.rlca_episodic_prefix_sum(x["x_i32"], x["terminated"], x["truncated"], out=o[0], **kw)
+
+
+def run_sweep(args):
+    """One JSON line per (estimator, E, T, layout, truncation): device time per
+    call from CUDA graphs of back-to-back calls on replicas whose footprint
+    exceeds 3 x L2, algorithmic bytes, achieved GB/s and fraction of peak."""
+    import torch
+    from first_order_linear_gb300 import build, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    peak, peak_kind = _peaks()
+    kinds = args.sweep_kinds.split(",") if args.sweep_kinds else SWEEP_KINDS
+    shapes = [(4096, 128, False, True), (4096, 256, False, False), (1024, 2048, False, False)]
+    shapes += [(E, T, tm, tr) for E in (256, 1024, 4096, 16384) for T in (32, 128, 512, 2048)
+               for tm in (False, True) for tr in (False, True)]
+    stream = torch.cuda.Stream(dev)
+    for kind in kinds:
+        for E, T, tm, trunc in shapes:
+            d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
+            foot = sum(v.numel() * v.element_size() for v in d.values() if isinstance(v, torch.Tensor))
+            foot += sum(E * T * 4 for _ in spec)
+            nb = max(2, min(64, math.ceil(3 * l2 / foot)))
+            src = {k: (synth.to_time_major(v) if tm and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+            reps = []
+            for i in range(nb):
+                x = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in src.items()}
+                o = [torch.empty(sh if not tm else (sh[1], sh[0]), dtype=dt, device=dev) for sh, dt in spec]
+                reps.append((x, o))
+            del src
+            with torch.cuda.stream(stream):
+                for x, o in reps:
+                    _sweep_call(kind, x, o, tm)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for x, o in reps:
+                    _sweep_call(kind, x, o, tm)
+            us_first = _graph_us(g, nb, stream, replays=2)
+            replays = max(3, min(200, int(20000 / max(1e-3, us_first * nb))))
+            us = _graph_us(g, nb, stream, replays=replays)
+            gbps = nbytes / (us / 1e6) / 1e9
+            print(json.dumps({"kind": kind, "E": E, "T": T, "layout": "time-major" if tm else "env-major",
+                              "trunc": trunc, "us_per_call": round(us, 3), "algorithmic_bytes": nbytes,
+                              "GBps": round(gbps, 1), "frac_of_peak": round(gbps / peak, 4),
+                              "peak": f"{peak} GB/s {peak_kind}", "env_steps_per_s": E * T / (us / 1e6),
+                              "replicas": nb}), flush=True)
+            del reps, g, d
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -461,9 +574,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one line per estimator and benchmark shape instead of the step metric")
+    ap.add_argument("--sweep-kinds", default="", help="comma-separated subset of " + ",".join(SWEEP_KINDS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

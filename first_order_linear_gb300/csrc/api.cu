@@ -167,10 +167,32 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   // one affine map per (row, segment): two values, two of each for the fused value targets
   const size_t ws_elem = kind == Kind::ValueTargets ? 16 : 8;
   q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
-  q.fast = !q.staged && !q.time_major && vec && T % kEmSteps == 0 && q.ntiles == 1 && q.nseg == 1 &&
-           !(flags & RLCA_MULTIPASS);
+  const bool fast_ok = !q.staged && !q.time_major && vec && q.nseg == 1 && !(flags & RLCA_MULTIPASS);
+  q.fast = fast_ok && T % kEmSteps == 0 && q.ntiles == 1;
+  q.steps = kEmSteps;
+  const int W8 = next_pow2((T + 7) / 8);
+  // Retrace's per-warp staging keeps fewer CTAs resident, so it switches only
+  // once four times as many threads are in flight
+  const int64_t l8_min_threads = (int64_t)sm_count * 1024 * (retrace ? 4 : 1);
+  if (fast_ok && T >= kFastL8MinT && T % 8 == 0 && (int64_t)E * (T / 8) >= l8_min_threads &&
+      W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
+    // long rows on enough environments: 8 steps per thread halves the warps per row
+    q.fast = true;
+    q.steps = 8;
+    q.ntiles = 1;
+    q.width = W8;
+    q.block = std::max(W8, kEmMinBlock);
+    q.rows_per_cta = q.block / W8;
+    q.tile = 8 * W8;
+    q.row_blocks = (E + q.rows_per_cta - 1) / q.rows_per_cta;
+    q.seg_len = q.tile;
+    q.smem_driver_bound = W8 > 32 ? (size_t)2 * q.rows_per_cta * (W8 / 32) * kMaxMapBytes : 0;
+    if (retrace)
+      q.smem = (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
+  }
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
+
   *out = q;
   return true;
 }

@@ -60,15 +60,24 @@ static cudaError_t launch_tm_c(const Plan& p, const Est& est, const Geom& g, cud
   }
 }
 
-template <class Est, int W>
-static cudaError_t launch_fast_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+template <class Est, int W, int LS>
+static cudaError_t launch_fast_wl(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if constexpr (W <= WidthCaps<Est>::em) {
-    using S = EmShape<W>;
+    using S = EmShape<W, LS>;
     const size_t drv = S::NWR > 1 ? (size_t)2 * S::ROWS * S::NWR * sizeof(Aff<typename Est::V>) : 0;
-    return launch_one<Est>(em_fast_kernel<Est, W>, p, drv + p.smem, est, g, s);
+    return launch_one<Est>(em_fast_kernel<Est, W, LS>, p, drv + p.smem, est, g, s);
   } else {
     return cudaErrorInvalidConfiguration;
   }
+}
+
+template <class Est, int W>
+static cudaError_t launch_fast_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if (p.steps == 8) {
+    if constexpr (W >= 64) return launch_fast_wl<Est, W, 8>(p, est, g, s);
+    return cudaErrorInvalidConfiguration;
+  }
+  return launch_fast_wl<Est, W, kEmSteps>(p, est, g, s);
 }
 
 template <class Est, int W>

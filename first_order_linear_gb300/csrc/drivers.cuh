@@ -162,14 +162,14 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
 // ---------------------------------------------------------------------------
 // fast env-major driver: the common case compiled without run-time
 // generality.  Preconditions (checked by the planner): 16-byte aligned rows,
-// T % kEmSteps == 0 and T <= TILE (one tile per row), one segment, one pass.
-// A thread therefore holds either all kEmSteps steps or none, and a thread
+// T % LS == 0 and T <= TILE (one tile per row), one segment, one pass.
+// A thread therefore holds either all LS steps or none, and a thread
 // beyond its row's end contributes the identity map to the scan.
 // ---------------------------------------------------------------------------
-template <class Est, int TPR>
-__global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
+template <class Est, int TPR, int LS>
+__global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
     em_fast_kernel(Est est, Geom g) {
-  using S = EmShape<TPR>;
+  using S = EmShape<TPR, LS>;
   using V = typename Est::V;
   constexpr bool BWD = Est::kBackward;
   constexpr int L = S::L, GW = S::GW, NWR = S::NWR;

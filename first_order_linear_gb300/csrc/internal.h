@@ -25,6 +25,7 @@ struct Plan {
   bool time_major;
   bool staged;      // env-major tiles staged through shared memory (es_scan_kernel)
   bool fast;        // env-major, one tile per row, one segment (em_fast_kernel)
+  int steps;        // steps per thread of the fast driver (kEmSteps or 8)
   int width;        // env-major: threads per row; time-major: chunk-threads per environment
   int block;        // threads per CTA
   int rows_per_cta;

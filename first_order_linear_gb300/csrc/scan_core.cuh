@@ -247,6 +247,13 @@ struct Geom {
 #endif
 constexpr int kEmSteps = RLCA_EM_STEPS;
 
+// rows of at least this many steps use 8 steps per thread in the fast
+// driver (half the warps per row)
+#ifndef RLCA_FAST_L8_MIN_T
+#define RLCA_FAST_L8_MIN_T 1024
+#endif
+constexpr int kFastL8MinT = RLCA_FAST_L8_MIN_T;
+
 // smallest env-major CTA (rows shorter than this share a CTA)
 #ifndef RLCA_EM_MIN_BLOCK
 #define RLCA_EM_MIN_BLOCK 128
@@ -254,9 +261,9 @@ constexpr int kEmSteps = RLCA_EM_STEPS;
 constexpr int kEmMinBlock = RLCA_EM_MIN_BLOCK;
 
 // env-major: TPR threads per row, kEmSteps steps per thread, rows packed kEmMinBlock threads per CTA
-template <int TPR>
+template <int TPR, int LS = kEmSteps>
 struct EmShape {
-  static constexpr int L = kEmSteps;
+  static constexpr int L = LS;
   static constexpr int TILE = TPR * L;
   static constexpr int BLOCK = TPR >= kEmMinBlock ? TPR : kEmMinBlock;
   static constexpr int ROWS = BLOCK / TPR;

@@ -99,6 +99,21 @@ def test_long_rows_few_envs_two_pass(kind, tm):
 
 
 @pytest.mark.parametrize("kind", parity.KINDS)
+@pytest.mark.parametrize("T", [1024, 3072, 4096])
+def test_long_single_tile_rows(kind, T):
+    """Rows of 1024-4096 steps fit one tile.  With few environments the fast
+    env-major driver runs them with 4 steps per thread; once E*T/8 threads
+    fill the GPU (four times that for Retrace) with 8 steps per thread.  Both
+    sides of that switch are checked, with a ragged environment count."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    need = sms * 1024 * (4 if kind == "retrace" else 1)
+    e_long = -(-need // (T // 8)) + 3
+    parity.check_case(kind, 70, T, seed=T + 3, p_term=0.01)
+    parity.check_case(kind, e_long, T, seed=T + 4, p_term=0.01)
+    parity.check_case(kind, e_long, T, seed=T + 5, p_term=0.01, inputs_ready=True)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
 def test_misaligned_pointers(kind):
     """Inputs and outputs at 4-byte (not 16-byte) offsets take the scalar
     load path and must give the same results."""
