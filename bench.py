@@ -458,6 +458,10 @@ def run_e2e(args, d_cpu, dev):
 # --------------------------------------------------------------------------
 
 SWEEP_KINDS = ("gae", "disc", "td", "vt", "vtrace", "retrace", "elig", "psum")
+# (E, T, time_major, truncation): the named configurations, then the E x T grid in both layouts
+SWEEP_SHAPES = [(4096, 128, False, True), (4096, 256, False, False), (1024, 2048, False, False)]
+SWEEP_SHAPES += [(E, T, tm, tr) for E in (256, 1024, 4096, 16384) for T in (32, 128, 512, 2048)
+                 for tm in (False, True) for tr in (False, True)]
 
 
 def _sweep_case(kind, E, T, trunc, dev):
@@ -527,9 +531,7 @@ def run_sweep(args):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     peak, peak_kind = _peaks()
     kinds = args.sweep_kinds.split(",") if args.sweep_kinds else SWEEP_KINDS
-    shapes = [(4096, 128, False, True), (4096, 256, False, False), (1024, 2048, False, False)]
-    shapes += [(E, T, tm, tr) for E in (256, 1024, 4096, 16384) for T in (32, 128, 512, 2048)
-               for tm in (False, True) for tr in (False, True)]
+    shapes = SWEEP_SHAPES
     stream = torch.cuda.Stream(dev)
     for kind in kinds:
         for E, T, tm, trunc in shapes:

@@ -190,6 +190,40 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     if (retrace)
       q.smem = (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
   }
+  // time-major rows of whole 8-step chunks with 32-bit element offsets take
+  // the fast time-major driver in one pass: 32 environments per CTA once that
+  // still leaves two CTAs per SM, else 8 (32-byte row pieces, 4x the CTAs).
+  // Few environments with many tiles each keep the segmented split instead.
+  const int ct_need = next_pow2((T + 7) / 8);
+  const int tf_ew = (E >= (int64_t)64 * sm_count || ct_need < 4) ? 32 : 8;
+  const int tf_ct = std::min(ct_need, tf_ew == 32 ? 16 : 32);
+  const int64_t tf_threads = (E + tf_ew - 1) / tf_ew * tf_ew * tf_ct;
+  const bool tf_few = q.nseg > 1 && tf_threads < (int64_t)sm_count * 128 && T > 4 * 8 * tf_ct;
+  if (q.time_major && !retrace && !tf_few && T % 8 == 0 && !(flags & RLCA_MULTIPASS) &&
+      (uint64_t)E * (uint64_t)T < (uint64_t{1} << 32)) {
+    // staged: 16-byte pieces of 128-byte step rows (32 environments, E % 4
+    // == 0, aligned inputs) through a ring of 64-step tiles.  With 8
+    // environments per CTA the rows are single 32-byte sectors and reading
+    // them straight into registers is faster.
+    const bool staged = kTmStaged && vec && E % 4 == 0 && tf_ew == 32;
+    const int EW = tf_ew, CT = staged ? std::min(tf_ct, tf_ew == 32 ? 8 : 32) : tf_ct;
+    q.tm_fast = true;
+    q.tm_staged = staged;
+    q.env_width = EW;
+    q.width = CT;
+    q.block = EW * CT;
+    q.rows_per_cta = EW;
+    q.tile = 8 * CT;
+    q.ntiles = (T + q.tile - 1) / q.tile;
+    q.nseg = 1;
+    q.seg_len = q.ntiles * q.tile;
+    q.row_blocks = (E + EW - 1) / EW;
+    q.smem = 0;
+    q.smem_driver_bound = (size_t)CT * (EW + 1) * (kMaxMapBytes + kMaxMapBytes / 2);
+    // the stages: at most 4 float and 2 flag inputs of CT * (8 * EW + EW) elements
+    if (staged) q.smem_driver_bound += (size_t)RLCA_TS_STAGES * ((size_t)CT * 9 * EW * 18 + 16);
+    q.ws_bytes = 0;
+  }
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
 

@@ -9,11 +9,13 @@ template <class Est>
 struct WidthCaps {
   static constexpr int em = kEmMaxWidth;
   static constexpr int tm = kTmMaxWidth;
+  static constexpr bool tm_fast = true;
 };
 template <bool H>
 struct WidthCaps<RetraceEst<H>> {
   static constexpr int em = kRetraceEmMaxWidth;
   static constexpr int tm = kRetraceTmMaxWidth;
+  static constexpr bool tm_fast = false;  // stages its per-action blocks per tile
 };
 
 // smem = the driver's exchange arrays (sized here from the same shape
@@ -80,6 +82,62 @@ static cudaError_t launch_fast_w(const Plan& p, const Est& est, const Geom& g, c
   return launch_fast_wl<Est, W, kEmSteps>(p, est, g, s);
 }
 
+template <class Est, int EW, int CT>
+static cudaError_t launch_tf(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (WidthCaps<Est>::tm_fast) {
+    return launch_one<Est>(tm_fast_kernel<Est, EW, CT>, p, tf_smem_bytes<typename Est::V, EW, CT>(), est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est, int EW, int CT>
+static cudaError_t launch_ts(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if constexpr (WidthCaps<Est>::tm_fast && Est::kStageable) {
+    return launch_one<Est>(tm_staged_kernel<Est, EW, CT>, p, ts_smem_bytes<Est, EW, CT>(), est, g, s);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est>
+static cudaError_t launch_ts_any(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if (p.env_width == 32) {
+    switch (p.width) {
+      case 1: return launch_ts<Est, 32, 1>(p, est, g, s);
+      case 2: return launch_ts<Est, 32, 2>(p, est, g, s);
+      case 4: return launch_ts<Est, 32, 4>(p, est, g, s);
+      case 8: return launch_ts<Est, 32, 8>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  return cudaErrorInvalidConfiguration;  // the planner stages 32-environment tiles only
+}
+
+template <class Est>
+static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+  if (p.env_width == 32) {
+    switch (p.width) {
+      case 1: return launch_tf<Est, 32, 1>(p, est, g, s);
+      case 2: return launch_tf<Est, 32, 2>(p, est, g, s);
+      case 4: return launch_tf<Est, 32, 4>(p, est, g, s);
+      case 8: return launch_tf<Est, 32, 8>(p, est, g, s);
+      case 16: return launch_tf<Est, 32, 16>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  if (p.env_width == 8) {
+    switch (p.width) {
+      case 4: return launch_tf<Est, 8, 4>(p, est, g, s);
+      case 8: return launch_tf<Est, 8, 8>(p, est, g, s);
+      case 16: return launch_tf<Est, 8, 16>(p, est, g, s);
+      case 32: return launch_tf<Est, 8, 32>(p, est, g, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
 template <class Est, int W>
 static cudaError_t launch_es_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if constexpr (kStagedPath && Est::kStageable && W <= kEsMaxWidth) {
@@ -121,6 +179,7 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
       default: return cudaErrorInvalidConfiguration;
     }
   }
+  if (p.tm_fast) return p.tm_staged ? launch_ts_any(p, est, g, s) : launch_tf_any(p, est, g, s);
   if (p.time_major) {
     switch (p.width) {
       case 1: return launch_tm_c<Est, 1>(p, est, g, s);

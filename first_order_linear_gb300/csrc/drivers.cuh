@@ -402,6 +402,276 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 }
 
 // ---------------------------------------------------------------------------
+// fast time-major driver.  Preconditions (checked by the planner): T % L == 0,
+// E * T < 2^32, one segment, one pass.  Each tile of CT * L steps: every
+// thread composes its chunk's L maps from coalesced step rows (EW
+// consecutive environments per load), the CT chunk maps of an environment are
+// scanned by CT adjacent lanes with shuffles (log2 CT rounds instead of a
+// serial walk), and the chunk boundary values come back through shared
+// memory.  The scan lanes of an environment keep its carry across tiles.
+// ---------------------------------------------------------------------------
+template <class Est, int EW, int CT>
+__global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK)
+    tm_fast_kernel(Est est, Geom g) {
+  using S = TfShape<EW, CT>;
+  using V = typename Est::V;
+  constexpr bool BWD = Est::kBackward;
+  constexpr int L = S::L, PAD = S::PAD;
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  Aff<V>* xs = reinterpret_cast<Aff<V>*>(smem);  // [CT][PAD] chunk maps
+  V* ys = reinterpret_cast<V*>(xs + CT * PAD);    // [CT][PAD] values entering each chunk
+
+  const int tid = threadIdx.x;
+  const int j = tid % EW, c = tid / EW;    // load / emit role
+  const int js = tid / CT, cs = tid % CT;  // scan role
+  const int64_t row0 = (int64_t)blockIdx.x * EW;
+  const int64_t row = row0 + j;
+  const bool row_ok = row < g.E;
+  const uint32_t E32 = (uint32_t)g.E;
+  const TimeMajor lay{g.E, g.T};
+  const bool early = g.early != 0;
+  if (!early) pdl_wait();
+
+  V carry = row0 + js < g.E ? est.row_carry(row0 + js) : V(0);
+  const int ntiles = (g.T + S::TILE - 1) / S::TILE;
+  for (int it = 0; it < ntiles; ++it) {
+    const int tile = BWD ? ntiles - 1 - it : it;
+    const int ts = tile * S::TILE;
+    const int t0 = ts + c * L;
+    const int n = (row_ok && t0 < g.T) ? L : 0;
+    const TmIO32 io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32};
+
+    typename Est::template Regs<L> R;
+    est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
+    if (it == ntiles - 1) pdl_trigger();
+    if constexpr (Est::kNb > 0) {
+      float got[Est::kNb > 0 ? Est::kNb : 1];
+#pragma unroll
+      for (int i = 0; i < Est::kNb; ++i) got[i] = 0.f;
+      const int tn = BWD ? t0 + L : t0 - 1;
+      if (n > 0 && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      est.nb_take(R, got);
+    }
+
+    Aff<V> cf[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) cf[k] = n != 0 ? est.coef(R, k, t0 + k) : aff_identity<V>();
+    Aff<V> agg = aff_identity<V>();
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) agg = compose(cf[k], agg);
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) agg = compose(cf[k], agg);
+    }
+    xs[c * PAD + j] = agg;
+    __syncthreads();
+
+    // scan role: inclusive scan of environment js's chunk maps in time order
+    // of application (suffix for a backward scan, prefix for a forward one)
+    Aff<V> m = xs[cs * PAD + js];
+#pragma unroll
+    for (int d = 1; d < CT; d <<= 1) {
+      if (BWD) {
+        const Aff<V> o = shfl_down_aff(m, d, CT);
+        if (cs + d < CT) m = compose(m, o);
+      } else {
+        const Aff<V> o = shfl_up_aff(m, d, CT);
+        if (cs >= d) m = compose(m, o);
+      }
+    }
+    Aff<V> ex = BWD ? shfl_down_aff(m, 1, CT) : shfl_up_aff(m, 1, CT);
+    if (cs == (BWD ? CT - 1 : 0)) ex = aff_identity<V>();
+    const Aff<V> tot = shfl_idx_aff(m, BWD ? 0 : CT - 1, CT);
+    ys[cs * PAD + js] = ex.a + ex.b * carry;
+    carry = tot.a + tot.b * carry;
+    __syncthreads();
+
+    V A = ys[c * PAD + j];
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    }
+    if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
+    est.template store<L>(R, io);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// staged time-major driver.  Preconditions: those of the fast time-major
+// driver, E % 4 == 0, 16-byte aligned float inputs and 4-byte aligned flag
+// inputs.  The inputs of the tiles stream into a ring of NS shared-memory
+// stages with cp.async (16-byte pieces of a step row for floats, 4-byte
+// pieces for flags), NS - 1 tiles ahead of the tile being scanned, so the
+// bytes in flight depend on neither registers nor occupancy.  The scan is
+// the fast time-major one; outputs go straight to global memory.
+// ---------------------------------------------------------------------------
+template <class Est, int EW, int CT>
+__global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK)
+    tm_staged_kernel(Est est, Geom g) {
+  using S = TsShape<EW, CT>;
+  using V = typename Est::V;
+  constexpr bool BWD = Est::kBackward;
+  constexpr int L = S::L, PAD = S::PAD, NS = S::NS, CS = S::CS, FB = S::FB;
+  constexpr int QR = EW / 4;            // 4-element pieces per step row
+  constexpr int PIECES = S::TILE * QR;  // pieces per staged input and tile
+  constexpr size_t STAGE = ts_stage_bytes<Est, EW, CT>();
+  static_assert(PIECES % S::BLOCK == 0, "whole copy rounds");
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  Aff<V>* xs = reinterpret_cast<Aff<V>*>(smem);  // [CT][PAD] chunk maps
+  V* ys = reinterpret_cast<V*>(xs + CT * PAD);    // [CT][PAD] values entering each chunk
+  unsigned char* ring = smem + align16(tf_smem_bytes<V, EW, CT>());
+
+  const int tid = threadIdx.x;
+  const int j = tid % EW, c = tid / EW;    // load / emit role
+  const int js = tid / CT, cs = tid % CT;  // scan role
+  const int64_t row0 = (int64_t)blockIdx.x * EW;
+  const int64_t row = row0 + j;
+  const bool row_ok = row < g.E;
+  const uint32_t E32 = (uint32_t)g.E;
+  const uint32_t e0 = (uint32_t)row0;
+  const TimeMajor lay{g.E, g.T};
+  const bool early = g.early != 0;
+  if (!early) pdl_wait();
+
+  StagedList in;
+  est.staged_io(in);
+  const int ntiles = (g.T + S::TILE - 1) / S::TILE;
+
+  // issue the copies of the it-th tile in processing order into stage it % NS
+  // (one commit group per call, empty past the last tile)
+  auto stage_tile = [&](int it) {
+    if (it < ntiles) {
+      const int ts = (BWD ? ntiles - 1 - it : it) * S::TILE;
+      unsigned char* st = ring + (size_t)(it % NS) * STAGE;
+#pragma unroll
+      for (int i = 0; i < PIECES / S::BLOCK; ++i) {
+        const int p = tid + i * S::BLOCK;
+        const int r = p / QR, q = p % QR;
+        const int t = ts + r;
+        const uint32_t e = e0 + 4u * (uint32_t)q;
+        if (t < g.T && e < E32) {  // E % 4 == 0: a piece is wholly inside or outside
+          const uint32_t go = (uint32_t)t * E32 + e;
+          const int so = (r / L) * CS + (r % L) * EW + 4 * q;
+#pragma unroll
+          for (int b = 0; b < Est::kSF; ++b)
+            cp_async16(reinterpret_cast<float*>(st) + b * FB + so, static_cast<const float*>(in.fin[b]) + go);
+#pragma unroll
+          for (int b = 0; b < Est::kSB; ++b)
+            if (in.bin[b] != nullptr) cp_async4(st + (size_t)4 * Est::kSF * FB + b * FB + so, in.bin[b] + go);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // the neighbour step's inputs of the it-th tile, loaded one tile ahead
+  constexpr int NB = Est::kNb > 0 ? Est::kNb : 1;
+  auto nb_fetch = [&](int it, float (&got)[NB]) {
+#pragma unroll
+    for (int i = 0; i < NB; ++i) got[i] = 0.f;
+    if (Est::kNb > 0 && it < ntiles) {
+      const int t0 = (BWD ? ntiles - 1 - it : it) * S::TILE + c * L;
+      const int tn = BWD ? t0 + L : t0 - 1;
+      if (row_ok && t0 < g.T && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < NS - 1; ++s) stage_tile(s);
+  float nb_cur[NB];
+  nb_fetch(0, nb_cur);
+  cp_async_wait<NS - 2>();
+  __syncthreads();
+
+  V carry = row0 + js < g.E ? est.row_carry(row0 + js) : V(0);
+  for (int it = 0; it < ntiles; ++it) {
+    stage_tile(it + NS - 1);  // into the stage every thread finished reading in iteration it - 1
+    float nb_nxt[NB];
+    nb_fetch(it + 1, nb_nxt);
+    if (it == ntiles - 1) pdl_trigger();
+    const int tile = BWD ? ntiles - 1 - it : it;
+    const int ts = tile * S::TILE;
+    const int t0 = ts + c * L;
+    const int n = (row_ok && t0 < g.T) ? L : 0;
+    const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
+    const TmSIO<EW, FB> io{reinterpret_cast<const float*>(st), st + (size_t)4 * Est::kSF * FB, c * CS + j, row, t0, n,
+                           (uint32_t)t0 * E32 + (uint32_t)row, E32};
+
+    typename Est::template Regs<L> R;
+    est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
+    if constexpr (Est::kNb > 0) est.nb_take(R, nb_cur);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) nb_cur[i] = nb_nxt[i];
+
+    Aff<V> cf[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) cf[k] = n != 0 ? est.coef(R, k, t0 + k) : aff_identity<V>();
+    Aff<V> agg = aff_identity<V>();
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) agg = compose(cf[k], agg);
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) agg = compose(cf[k], agg);
+    }
+    xs[c * PAD + j] = agg;
+    __syncthreads();
+
+    Aff<V> m = xs[cs * PAD + js];
+#pragma unroll
+    for (int d = 1; d < CT; d <<= 1) {
+      if (BWD) {
+        const Aff<V> o = shfl_down_aff(m, d, CT);
+        if (cs + d < CT) m = compose(m, o);
+      } else {
+        const Aff<V> o = shfl_up_aff(m, d, CT);
+        if (cs >= d) m = compose(m, o);
+      }
+    }
+    Aff<V> ex = BWD ? shfl_down_aff(m, 1, CT) : shfl_up_aff(m, 1, CT);
+    if (cs == (BWD ? CT - 1 : 0)) ex = aff_identity<V>();
+    const Aff<V> tot = shfl_idx_aff(m, BWD ? 0 : CT - 1, CT);
+    ys[cs * PAD + js] = ex.a + ex.b * carry;
+    carry = tot.a + tot.b * carry;
+    cp_async_wait<NS - 2>();  // this thread's copies of tile it + 1 have landed
+    __syncthreads();          // ... everyone's, and the chunk entry values are visible
+
+    V A = ys[c * PAD + j];
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    }
+    if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
+    est.template store<L>(R, io);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // staged env-major driver
 //
 // For 16-byte aligned env-major rows (T % 4 == 0).  Each tile of the CTA's

@@ -25,8 +25,11 @@ struct Plan {
   bool time_major;
   bool staged;      // env-major tiles staged through shared memory (es_scan_kernel)
   bool fast;        // env-major, one tile per row, one segment (em_fast_kernel)
+  bool tm_fast;     // time-major, T % 8 == 0, E * T < 2^32, one segment (tm_fast_kernel)
+  bool tm_staged;   // ... and inputs staged through shared memory (tm_staged_kernel)
   int steps;        // steps per thread of the fast driver (kEmSteps or 8)
   int width;        // env-major: threads per row; time-major: chunk-threads per environment
+  int env_width;    // fast time-major: environments per CTA (8 or 32)
   int block;        // threads per CTA
   int rows_per_cta;
   int tile;         // steps per tile
@@ -43,6 +46,13 @@ struct Plan {
 // vec: the env-major arrays are 16-byte aligned (4-byte for flags) and
 // T % 4 == 0, so rows can be read as 16-byte vectors.
 bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec, Plan* p);
+
+#ifndef RLCA_TM_STAGED
+#define RLCA_TM_STAGED 1
+#endif
+// build-time choice: aligned time-major inputs stream through shared memory
+// (tm_staged_kernel) rather than straight into registers (tm_fast_kernel)
+constexpr bool kTmStaged = RLCA_TM_STAGED != 0;
 
 #ifndef RLCA_STAGED_PATH
 #define RLCA_STAGED_PATH 0

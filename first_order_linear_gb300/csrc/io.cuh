@@ -2,7 +2,9 @@
 //
 // Estimator functors read their L consecutive steps and write their outputs
 // through an I/O object, so the same functor serves
-//   GIO: global memory (the direct env-major and time-major drivers), and
+//   GIO: global memory (the direct env-major and time-major drivers),
+//   TmIO32: global memory, time-major, 32-bit offsets (fast time-major driver),
+//   TmSIO: shared-memory stages of the staged time-major driver, and
 //   SIO: shared memory staged by the CTA with coalesced async copies (the
 //        staged env-major driver; see staged.cuh).
 // Inputs are addressed by (index, pointer): the index is the position in the
@@ -45,6 +47,105 @@ struct GIO {
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* p, const uint32_t (&v)[L]) const {
     if (p != nullptr) store_ints<L>(p, lay, row, t0, n, vec(), v);
+  }
+};
+
+// Time-major [T, E] global I/O of the fast time-major driver: a thread's L
+// steps are either all in range (n == L) or none (n == 0), and every array's
+// element (t0 + k, row) sits at element offset off + k * E, computed in 32
+// bits (the planner takes this path only when E * T < 2^32).
+struct TmIO32 {
+  static constexpr bool kTimeMajor = true;
+  int64_t row;
+  int t0;
+  int n;
+  uint32_t off;  // t0 * E + row
+  uint32_t E;
+
+  __device__ __forceinline__ uint32_t o(int k) const { return off + (uint32_t)k * E; }
+  __device__ __forceinline__ int64_t at(int k) const { return (int64_t)o(k); }
+  template <int L>
+  __device__ __forceinline__ void f(int, const float* __restrict__ p, float (&v)[L]) const {
+#pragma unroll
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? __ldg(p + o(k)) : 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void i(int, const int32_t* __restrict__ p, uint32_t (&v)[L]) const {
+#pragma unroll
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? (uint32_t)__ldg(p + o(k)) : 0u;
+  }
+  template <int L>
+  __device__ __forceinline__ uint32_t flags(int, const uint8_t* __restrict__ p) const {
+    if (p == nullptr || n == 0) return 0u;
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int k = 0; k < L; ++k) bits |= (uint32_t)(__ldg(p + o(k)) != 0) << k;
+    return bits;
+  }
+  template <int L>
+  __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
+    if (p == nullptr || n == 0) return;
+#pragma unroll
+    for (int k = 0; k < L; ++k) p[o(k)] = v[k];
+  }
+  template <int L>
+  __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {
+    if (p == nullptr || n == 0) return;
+#pragma unroll
+    for (int k = 0; k < L; ++k) p[o(k)] = (int32_t)v[k];
+  }
+};
+
+// Time-major I/O of the staged time-major driver: inputs from the current
+// shared-memory stage (float input b at fbuf + b * FB, flag input b at
+// bbuf + b * FB; the thread's step k at slot + k * EW), outputs and the rare
+// truncation-value loads straight to global memory as in TmIO32.
+template <int EW, int FB>
+struct TmSIO {
+  static constexpr bool kTimeMajor = true;
+  const float* fbuf;
+  const uint8_t* bbuf;
+  int slot;
+  int64_t row;
+  int t0;
+  int n;
+  uint32_t off;  // t0 * E + row
+  uint32_t E;
+
+  __device__ __forceinline__ uint32_t o(int k) const { return off + (uint32_t)k * E; }
+  __device__ __forceinline__ int64_t at(int k) const { return (int64_t)o(k); }
+  template <int L>
+  __device__ __forceinline__ void f(int idx, const float*, float (&v)[L]) const {
+    const float* s = fbuf + idx * FB + slot;
+#pragma unroll
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? s[k * EW] : 0.f;
+  }
+  template <int L>
+  __device__ __forceinline__ void i(int idx, const int32_t*, uint32_t (&v)[L]) const {
+    const uint32_t* s = reinterpret_cast<const uint32_t*>(fbuf + idx * FB + slot);
+#pragma unroll
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? s[k * EW] : 0u;
+  }
+  template <int L>
+  __device__ __forceinline__ uint32_t flags(int idx, const uint8_t* p) const {
+    if (p == nullptr || n == 0) return 0u;
+    const uint8_t* s = bbuf + idx * FB + slot;
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int k = 0; k < L; ++k) bits |= (uint32_t)(s[k * EW] != 0) << k;
+    return bits;
+  }
+  template <int L>
+  __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
+    if (p == nullptr || n == 0) return;
+#pragma unroll
+    for (int k = 0; k < L; ++k) p[o(k)] = v[k];
+  }
+  template <int L>
+  __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {
+    if (p == nullptr || n == 0) return;
+#pragma unroll
+    for (int k = 0; k < L; ++k) p[o(k)] = (int32_t)v[k];
   }
 };
 

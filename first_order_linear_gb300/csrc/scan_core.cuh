@@ -312,6 +312,12 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// waits until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 // time-major: 32 environments per warp, C chunk-threads per environment, L steps each
 template <int C>
@@ -321,6 +327,48 @@ struct TmShape {
   static constexpr int BLOCK = EW * C;
   static constexpr int TILE = C * L;
 };
+
+// fast time-major: EW environments per CTA (EW consecutive floats of a step
+// row per load), CT chunk-threads per environment, L steps each.  Thread tid
+// loads and emits environment tid % EW, chunk tid / EW; for the scan across
+// chunks it takes environment tid / CT, chunk tid % CT, so an environment's
+// CT chunk maps sit in CT adjacent lanes of one warp.
+template <int EW, int CT>
+struct TfShape {
+  static constexpr int L = 8;
+  static constexpr int BLOCK = EW * CT;
+  static constexpr int TILE = CT * L;
+  static constexpr int PAD = EW + 1;  // row stride of the [CT][EW] exchange arrays
+  static_assert(BLOCK % 32 == 0 && CT <= 32 && (CT & (CT - 1)) == 0, "chunk groups tile the warps");
+};
+template <class V, int EW, int CT>
+__host__ __device__ constexpr size_t tf_smem_bytes() {
+  return (size_t)CT * TfShape<EW, CT>::PAD * (sizeof(Aff<V>) + sizeof(V));
+}
+
+// staged time-major: the fast time-major shape with its inputs copied into
+// a ring of NS shared-memory stages, one tile per stage.  In a stage each
+// staged input is a [CT][CS] buffer: chunk c's step k, environment j at
+// c * CS + k * EW + j.  CS pads a chunk by EW elements when several chunks
+// share a warp (EW < 32), so their lanes read distinct banks.
+#ifndef RLCA_TS_STAGES
+#define RLCA_TS_STAGES 2
+#endif
+template <int EW, int CT>
+struct TsShape : TfShape<EW, CT> {
+  static constexpr int NS = RLCA_TS_STAGES;
+  static constexpr int CS = TfShape<EW, CT>::L * EW + (EW < 32 ? EW : 0);
+  static constexpr int FB = CT * CS;  // elements per staged buffer
+  static_assert(EW % 4 == 0 && CS % 4 == 0, "16-byte pieces of step rows");
+};
+template <class Est, int EW, int CT>
+__host__ __device__ constexpr size_t ts_stage_bytes() {
+  return align16((size_t)TsShape<EW, CT>::FB * (4 * Est::kSF + Est::kSB));
+}
+template <class Est, int EW, int CT>
+__host__ __device__ constexpr size_t ts_smem_bytes() {
+  return align16(tf_smem_bytes<typename Est::V, EW, CT>()) + TsShape<EW, CT>::NS * ts_stage_bytes<Est, EW, CT>();
+}
 
 // value at a segment's far edge: the row's carry pushed through the maps of
 // the segments between it and the row's end (written by the first pass of

@@ -58,6 +58,21 @@ def _tm(d, time_major):
     return {k: (synth.to_time_major(v) if time_major and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
+def _shift(d):
+    """Copies of the [.., T, ..] tensors one element past an aligned base:
+    4-byte (1-byte for flags) rather than 16-byte aligned."""
+    out = {}
+    for k, v in d.items():
+        if isinstance(v, torch.Tensor) and v.dim() >= 2:
+            buf = torch.empty(v.numel() + 16, dtype=v.dtype, device=v.device)
+            view = buf[1:1 + v.numel()].view(v.shape)
+            view.copy_(v)
+            out[k] = view
+        else:
+            out[k] = v
+    return out
+
+
 def _back(t, time_major):
     return synth.from_time_major(t) if time_major else t
 
@@ -85,11 +100,14 @@ def make_inputs(kind, E, T, seed, trunc, device, **kw):
     raise ValueError(kind)
 
 
-def run_gpu(kind, d, time_major=False, multipass=False, params=None, inputs_ready=False):
-    """Outputs of the CUDA path as env-major tensors (tuple)."""
+def run_gpu(kind, d, time_major=False, multipass=False, params=None, inputs_ready=False, shift=False):
+    """Outputs of the CUDA path as env-major tensors (tuple).  shift: pass
+    the inputs, in the call's layout, at unaligned addresses."""
     p = dict(gamma=GAMMA, lambda_=LAMBDA)
     p.update(params or {})
     x = _tm(d, time_major)
+    if shift:
+        x = _shift(x)
     common = dict(time_major=time_major, multipass=multipass, inputs_ready=inputs_ready)
     if kind == "gae":
         out = rlca.rlca_gae(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
@@ -168,11 +186,12 @@ def run_oracle(kind, d, rows, params=None):
 
 
 def check_case(kind, E, T, seed=0, trunc=True, time_major=False, multipass=False, params=None, device="cuda",
-               gen_device=None, rows=None, inputs=None, inputs_ready=False, **gen_kw):
+               gen_device=None, rows=None, inputs=None, inputs_ready=False, shift=False, **gen_kw):
     """Run one parity case; returns the worst relative error seen."""
     d = inputs if inputs is not None else make_inputs(kind, E, T, seed, trunc, gen_device or device, **gen_kw)
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    got = run_gpu(kind, d, time_major=time_major, multipass=multipass, params=params, inputs_ready=inputs_ready)
+    got = run_gpu(kind, d, time_major=time_major, multipass=multipass, params=params, inputs_ready=inputs_ready,
+                  shift=shift)
     torch.cuda.synchronize()
     if rows is None:
         rows = sample_rows(E, T, seed)

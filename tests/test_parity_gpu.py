@@ -99,6 +99,22 @@ def test_long_rows_few_envs_two_pass(kind, tm):
 
 
 @pytest.mark.parametrize("kind", parity.KINDS)
+@pytest.mark.parametrize("T", [8, 16, 24, 32, 64, 128, 256, 520, 2048])
+def test_time_major_chunk_groups(kind, T):
+    """Time-major rows of whole 8-step chunks run the fast time-major drivers
+    (direct or staged): 8 environments per CTA below 64 x SMs environments,
+    32 from there on, with 1 to 32 chunk lanes per environment; ragged E on
+    both sides."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 32 environments per CTA and E % 4 == 0 stream through shared-memory stages; the rest read
+    # straight into registers
+    for E, seed in ((13, 1), (12, 2), (64 * sms + 5, 3), (64 * sms + 4, 4)):
+        parity.check_case(kind, E, T, seed=T * 11 + seed, time_major=True, p_term=0.02)
+    for E, seed in ((13, 5), (12, 6)):
+        parity.check_case(kind, E, T, seed=T * 11 + seed, time_major=True, p_term=0.02, inputs_ready=True)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
 @pytest.mark.parametrize("T", [1024, 3072, 4096])
 def test_long_single_tile_rows(kind, T):
     """Rows of 1024-4096 steps fit one tile.  With few environments the fast
@@ -113,22 +129,14 @@ def test_long_single_tile_rows(kind, T):
     parity.check_case(kind, e_long, T, seed=T + 5, p_term=0.01, inputs_ready=True)
 
 
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
 @pytest.mark.parametrize("kind", parity.KINDS)
-def test_misaligned_pointers(kind):
-    """Inputs and outputs at 4-byte (not 16-byte) offsets take the scalar
-    load path and must give the same results."""
-    E, T = 37, 96
-    d = parity.make_inputs(kind, E, T, seed=5, trunc=True, device="cuda", p_term=0.05)
-    shifted = {}
-    for k, v in d.items():
-        if isinstance(v, torch.Tensor) and v.dim() >= 2:
-            buf = torch.empty(v.numel() + 16, dtype=v.dtype, device=v.device)
-            view = buf[1:1 + v.numel()].view(v.shape)
-            view.copy_(v)
-            shifted[k] = view
-        else:
-            shifted[k] = v
-    parity.check_case(kind, E, T, inputs=shifted)
+def test_misaligned_pointers(kind, tm):
+    """Inputs at 4-byte (flags: 1-byte) rather than 16-byte offsets take the
+    unstaged scalar load paths and must give the same results; E = 36 and
+    T = 96 would otherwise take the vector / staged paths."""
+    parity.check_case(kind, 36, 96, seed=5, p_term=0.05, time_major=tm, shift=True)
+    parity.check_case(kind, 37, 96, seed=6, p_term=0.05, time_major=tm, shift=True)
 
 
 @pytest.mark.parametrize("kind", ["gae", "disc", "td", "vt", "vtrace", "retrace"])
