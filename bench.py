@@ -568,6 +568,27 @@ def run_sweep(args):
     return 0
 
 
+def run_ncu_case(args):
+    """Four calls of one estimator on one seeded batch and nothing else: the
+    command line ncu captures (``--ncu-case vt,4096,128,em`` -> launches 0..3,
+    capture with ``-s 2 -c 1``)."""
+    import torch
+    from first_order_linear_gb300 import build, synth
+    kind, E, T, lay = args.ncu_case.split(",")
+    E, T, tm = int(E), int(T), lay == "tm"
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d, nbytes, spec = _sweep_case(kind, E, T, True, dev)
+    x = {k: (synth.to_time_major(v) if tm and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    o = [torch.empty(sh if not tm else (sh[1], sh[0]), dtype=dt, device=dev) for sh, dt in spec]
+    for _ in range(4):
+        _sweep_call(kind, x, o, tm)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": args.ncu_case, "algorithmic_bytes_per_call": nbytes}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,9 +600,13 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="print one line per estimator and benchmark shape instead of the step metric")
     ap.add_argument("--sweep-kinds", default="", help="comma-separated subset of " + ",".join(SWEEP_KINDS))
+    ap.add_argument("--ncu-case", default="",
+                    help="KIND,E,T,em|tm: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.ncu_case:
+        return run_ncu_case(args)
     if args.sweep:
         return run_sweep(args)
     if args.impl == "reference":
