@@ -378,9 +378,28 @@ def run_ours(args):
     n_trunc = int(d_cpu["truncated"].sum())
     fused_bytes = E * T * (4 + 4 + 1 + 1 + 4 * 4) + 32 * n_trunc + 4 * E
     peak, peak_kind = _peaks()
+    # context, not the path: a plain torch device copy moving the same bytes
+    # per launch (half read, half written), captured and replayed the same
+    # way over replicas larger than 3 x L2 -- what one launch of this size
+    # reaches on this machine
+    n_copy = fused_bytes // 8
+    srcs = [torch.zeros(n_copy, device=dev) for _ in range(nb)]
+    dsts = [torch.empty(n_copy, device=dev) for _ in range(nb)]
+    with torch.cuda.stream(stream):
+        for a_, b_ in zip(srcs, dsts):
+            b_.copy_(a_)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for a_, b_ in zip(srcs, dsts):
+            b_.copy_(a_)
+    us_copy = _graph_us(g, nb, stream)
+    kern["torch_copy_same_bytes"] = {"us_per_launch": us_copy, "bytes_per_launch": 8 * n_copy,
+                                     "frac_of_peak": 8 * n_copy / (us_copy / 1e6) / 1e9 / peak}
+    del g, srcs, dsts
     avg_us = ms_per_step * 1e3
     achieved = fused_bytes / (avg_us / 1e6) / 1e9
-    roofline = {"bound": "hbm", "kernel": "em_fast_kernel<ValueTargetsEst<true>,32> (rlca_value_targets)",
+    roofline = {"bound": "hbm", "kernel": "em_fast_kernel<ValueTargetsEst<true>,32,4> (rlca_value_targets)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "traffic": _recorded_traffic(),
                 "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_us": avg_us,
@@ -494,9 +513,9 @@ def _sweep_case(kind, E, T, trunc, dev):
     return d, per_step * E * T + tv_bytes, spec
 
 
-def _sweep_call(kind, x, o, tm):
+def _sweep_call(kind, x, o, tm, ready=False):
     from first_order_linear_gb300 import rlca
-    kw = dict(time_major=tm)
+    kw = dict(time_major=tm, inputs_ready=ready)
     b = (x.get("terminated"), x.get("truncated"), x.get("trunc_value"), x.get("bootstrap"))
     if kind == "gae":
         rlca.rlca_gae(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, advantages=o[0], returns=o[1], **kw)
@@ -522,7 +541,9 @@ def _sweep_call(kind, x, o, tm):
 def run_sweep(args):
     """One JSON line per (estimator, E, T, layout, truncation): device time per
     call from CUDA graphs of back-to-back calls on replicas whose footprint
-    exceeds 3 x L2, algorithmic bytes, achieved GB/s and fraction of peak."""
+    exceeds 3 x L2, algorithmic bytes, achieved GB/s and fraction of peak;
+    once in plain stream order and once with RLCA_INPUTS_READY (consecutive
+    calls on independent replicas overlap)."""
     import torch
     from first_order_linear_gb300 import build, synth
     build.build()
@@ -550,20 +571,30 @@ def run_sweep(args):
                 for x, o in reps:
                     _sweep_call(kind, x, o, tm)
             stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for x, o in reps:
-                    _sweep_call(kind, x, o, tm)
-            us_first = _graph_us(g, nb, stream, replays=2)
-            replays = max(3, min(200, int(20000 / max(1e-3, us_first * nb))))
-            us = _graph_us(g, nb, stream, replays=replays)
+            times = {}
+            for ready in (False, True):
+                with torch.cuda.stream(stream):
+                    _sweep_call(kind, reps[0][0], reps[0][1], tm, ready)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for x, o in reps:
+                        _sweep_call(kind, x, o, tm, ready)
+                us_first = _graph_us(g, nb, stream, replays=2)
+                replays = max(3, min(200, int(20000 / max(1e-3, us_first * nb))))
+                times[ready] = _graph_us(g, nb, stream, replays=replays)
+                del g
+            us, us_ready = times[False], times[True]
             gbps = nbytes / (us / 1e6) / 1e9
+            gbps_ready = nbytes / (us_ready / 1e6) / 1e9
             print(json.dumps({"kind": kind, "E": E, "T": T, "layout": "time-major" if tm else "env-major",
                               "trunc": trunc, "us_per_call": round(us, 3), "algorithmic_bytes": nbytes,
                               "GBps": round(gbps, 1), "frac_of_peak": round(gbps / peak, 4),
+                              "us_per_call_inputs_ready": round(us_ready, 3),
+                              "frac_of_peak_inputs_ready": round(gbps_ready / peak, 4),
                               "peak": f"{peak} GB/s {peak_kind}", "env_steps_per_s": E * T / (us / 1e6),
                               "replicas": nb}), flush=True)
-            del reps, g, d
+            del reps, d
             torch.cuda.empty_cache()
     return 0
 

@@ -479,27 +479,30 @@ struct RetraceStage {
   float lambda;
 
   // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous);
-  // item s writes its three scalars at index `slot` of the dst arrays
+  // item s writes its three scalars at index `slot` of the dst arrays.  The
+  // warp's Q and pi blocks go to shared memory as asynchronous 4-byte copies,
+  // all in flight at once (one memory round trip per chunk, no registers
+  // held), while the taken action and mu(a_t) load alongside.
   __device__ __forceinline__ void chunk(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p, float* dst_ev,
                                         float* dst_qa, float* dst_c, int slot) const {
     const float* qb = q + e0 * A;
     const float* pb = pi + e0 * A;
     const int total = cnt * A;
-#pragma unroll 6
     for (int f = lane; f < total; f += 32) {
-      raw_q[f] = __ldg(qb + f);
-      raw_p[f] = __ldg(pb + f);
+      cp_async4(raw_q + f, qb + f);
+      cp_async4(raw_p + f, pb + f);
     }
+    int at = lane < cnt ? __ldg(act + e0 + lane) : 0;
+    const float mu = lane < cnt ? __ldg(mu_a + e0 + lane) : 1.f;
+    cp_async_wait_all();
     __syncwarp();
     if (lane < cnt) {
       const float* rq = raw_q + lane * A;
       const float* rp = raw_p + lane * A;
       float ev = 0.f;
       for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
-      int at = __ldg(act + e0 + lane);
       at = at < 0 ? 0 : (at >= A ? A - 1 : at);
       const float pa = rp[at];
-      const float mu = __ldg(mu_a + e0 + lane);
       dst_ev[slot] = ev;
       dst_qa[slot] = rq[at];
       dst_c[slot] = lambda * fminf(1.f, pa / mu);

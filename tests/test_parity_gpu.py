@@ -98,6 +98,15 @@ def test_long_rows_few_envs_two_pass(kind, tm):
     parity.check_case(kind, 3, 40000, seed=11, time_major=tm)
 
 
+@pytest.mark.parametrize("kind", ["gae", "vt", "retrace", "elig", "psum_i32", "affine_fwd"])
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
+def test_rows_beyond_131072_steps(kind, tm):
+    """Rows longer than the 131072-step limit of the pages' fused kernels
+    (their backward-only unfused fallback beyond it) run the segmented
+    two-pass path, backward and forward alike."""
+    parity.check_case(kind, 2, 140_001, seed=17, time_major=tm, p_term=0.0005)
+
+
 @pytest.mark.parametrize("kind", parity.KINDS)
 @pytest.mark.parametrize("T", [8, 16, 24, 32, 64, 128, 256, 520, 2048])
 def test_time_major_chunk_groups(kind, T):
