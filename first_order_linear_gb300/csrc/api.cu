@@ -128,12 +128,17 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     const int cmax = retrace ? kRetraceTmMaxWidth : kTmMaxWidth;
     int C = (int)std::min<int64_t>(next_pow2((T + 7) / 8), cmax);
     if (flags & RLCA_MULTIPASS) C = std::max(1, C / 4);
+    // Retrace's per-warp staging grows with A: fewer chunk warps when it would not fit
+    while (retrace && C > 1 &&
+           (size_t)C * retrace_raw_floats(num_actions, true) * 4 + (size_t)3 * (8 * C + 1) * 32 * 4 +
+                   (size_t)2 * C * 32 * kMaxMapBytes > kMaxSmemPerCta)
+      C /= 2;
     q.width = C;
     q.block = 32 * C;
     q.rows_per_cta = 32;
     q.tile = 8 * C;
     q.smem_driver_bound = (size_t)2 * C * 32 * kMaxMapBytes;
-    q.smem = retrace ? (size_t)C * 64 * num_actions * 4 + (size_t)3 * (q.tile + 1) * 32 * 4 : 0;
+    q.smem = retrace ? (size_t)C * retrace_raw_floats(num_actions, true) * 4 + (size_t)3 * (q.tile + 1) * 32 * 4 : 0;
   } else {
     const int wmax = retrace ? kRetraceEmMaxWidth : kEmMaxWidth;
     int W = (int)std::min<int64_t>(next_pow2(std::max<int64_t>((T + kEmSteps - 1) / kEmSteps, kEmMinWidth)),
@@ -145,7 +150,8 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.tile = kEmSteps * W;
     const int nwr = W > 32 ? W / 32 : 1;
     q.smem_driver_bound = nwr > 1 ? (size_t)2 * q.rows_per_cta * nwr * kMaxMapBytes : 0;
-    q.smem = retrace ? (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4
+    q.smem = retrace ? (size_t)(q.block / 32) * retrace_raw_floats(num_actions, false) * 4 +
+                         (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4
                      : 0;
   }
   q.ntiles = (int)((T + q.tile - 1) / q.tile);
@@ -188,7 +194,8 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.seg_len = q.tile;
     q.smem_driver_bound = W8 > 32 ? (size_t)2 * q.rows_per_cta * (W8 / 32) * kMaxMapBytes : 0;
     if (retrace)
-      q.smem = (size_t)(q.block / 32) * 64 * num_actions * 4 + (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
+      q.smem = (size_t)(q.block / 32) * retrace_raw_floats(num_actions, false) * 4 +
+               (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
   }
   // time-major rows of whole 8-step chunks with 32-bit element offsets take
   // the fast time-major driver in one pass: 32 environments per CTA once that

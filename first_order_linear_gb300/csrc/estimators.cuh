@@ -470,6 +470,16 @@ struct VtraceEst : NoStage {
 // shared memory with coalesced loads; each tile stages its steps plus the
 // first step after it (the last step's successor).
 // ===========================================================================
+// per-warp raw Q / pi buffers of the Retrace staging: 1 = one 32-step chunk
+// at a time, 2 = the next chunk's copies in flight while this one reduces.
+// Env-major rows keep one (more CTAs resident measured faster); time-major
+// tiles, with few CTAs of up to 8 warps, take two.
+__host__ __device__ constexpr int retrace_bufs(bool time_major) { return time_major ? 2 : 1; }
+// floats of shared memory per warp for the raw blocks: buffers x (Q, pi) x 32 steps x A
+__host__ __device__ constexpr int retrace_raw_floats(int A, bool time_major) {
+  return retrace_bufs(time_major) * 64 * A;
+}
+
 struct RetraceStage {
   const float* q;
   const float* pi;
@@ -478,13 +488,15 @@ struct RetraceStage {
   int A;
   float lambda;
 
-  // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous);
-  // item s writes its three scalars at index `slot` of the dst arrays.  The
+  struct Pending {
+    int at;
+    float mu;
+  };
+  // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous): the
   // warp's Q and pi blocks go to shared memory as asynchronous 4-byte copies,
-  // all in flight at once (one memory round trip per chunk, no registers
-  // held), while the taken action and mu(a_t) load alongside.
-  __device__ __forceinline__ void chunk(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p, float* dst_ev,
-                                        float* dst_qa, float* dst_c, int slot) const {
+  // all in flight at once and committed as one group; the taken action and
+  // mu(a_t) load into registers alongside
+  __device__ __forceinline__ Pending issue(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p) const {
     const float* qb = q + e0 * A;
     const float* pb = pi + e0 * A;
     const int total = cnt * A;
@@ -492,22 +504,75 @@ struct RetraceStage {
       cp_async4(raw_q + f, qb + f);
       cp_async4(raw_p + f, pb + f);
     }
-    int at = lane < cnt ? __ldg(act + e0 + lane) : 0;
-    const float mu = lane < cnt ? __ldg(mu_a + e0 + lane) : 1.f;
-    cp_async_wait_all();
-    __syncwarp();
+    cp_async_commit();
+    Pending pd;
+    pd.at = lane < cnt ? __ldg(act + e0 + lane) : 0;
+    pd.mu = lane < cnt ? __ldg(mu_a + e0 + lane) : 1.f;
+    return pd;
+  }
+  // once the chunk's copies have landed: item `lane` writes its three
+  // scalars at index `slot` of the dst arrays
+  __device__ __forceinline__ void finish(const Pending& pd, int cnt, int lane, const float* raw_q,
+                                         const float* raw_p, float* dst_ev, float* dst_qa, float* dst_c,
+                                         int slot) const {
     if (lane < cnt) {
       const float* rq = raw_q + lane * A;
       const float* rp = raw_p + lane * A;
       float ev = 0.f;
       for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
-      at = at < 0 ? 0 : (at >= A ? A - 1 : at);
-      const float pa = rp[at];
+      const int at = pd.at < 0 ? 0 : (pd.at >= A ? A - 1 : pd.at);
       dst_ev[slot] = ev;
       dst_qa[slot] = rq[at];
-      dst_c[slot] = lambda * fminf(1.f, pa / mu);
+      dst_c[slot] = lambda * fminf(1.f, rp[at] / pd.mu);
     }
-    __syncwarp();
+  }
+  // walks chunks warp, warp + NW, ... < nch; where(ch, &e0, &cnt, &slot)
+  // locates a chunk (false: nothing to stage).  With two buffers the next
+  // chunk's copies are issued before waiting on the current one.
+  template <int NBUF, class Where>
+  __device__ __forceinline__ void walk(int nch, int warp, int NW, int lane, float* raw, float* s_ev, float* s_qa,
+                                       float* s_c, Where where) const {
+    const int blk = 32 * A;
+    auto buf = [&](int k) { return raw + (NBUF == 2 ? (k & 1) : 0) * 2 * blk; };
+    int64_t e0 = 0;
+    int cnt = 0, slot = 0;
+    Pending cur = {0, 1.f};
+    bool cur_ok = false;
+    if (NBUF == 2 && warp < nch) {
+      cur_ok = where(warp, &e0, &cnt, &slot);
+      if (cur_ok) cur = issue(e0, cnt, lane, buf(0), buf(0) + blk);
+    }
+    int k = 0;
+    for (int ch = warp; ch < nch; ch += NW, ++k) {
+      if (NBUF == 2) {
+        const int nx = ch + NW;
+        int64_t ne0 = 0;
+        int ncnt = 0, nslot = 0;
+        const bool nx_ok = nx < nch && where(nx, &ne0, &ncnt, &nslot);
+        Pending nxt = {0, 1.f};
+        if (nx_ok) {
+          nxt = issue(ne0, ncnt, lane, buf(k + 1), buf(k + 1) + blk);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+        __syncwarp();
+        if (cur_ok) finish(cur, cnt, lane, buf(k), buf(k) + blk, s_ev, s_qa, s_c, slot);
+        __syncwarp();
+        cur = nxt;
+        cur_ok = nx_ok;
+        e0 = ne0;
+        cnt = ncnt;
+        slot = nslot;
+      } else {
+        if (!where(ch, &e0, &cnt, &slot)) continue;
+        const Pending pd = issue(e0, cnt, lane, raw, raw + blk);
+        cp_async_wait<0>();
+        __syncwarp();
+        finish(pd, cnt, lane, raw, raw + blk, s_ev, s_qa, s_c, slot);
+        __syncwarp();
+      }
+    }
   }
 };
 
@@ -531,8 +596,8 @@ struct RetraceEst {
   };
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
 
-  // shared memory: per warp raw Q and pi blocks [32 * A] each, then the
-  // staged per-step scalars [3][ROWS][tile + 1]
+  // shared memory: per warp the raw Q and pi blocks (retrace_raw_floats),
+  // then the staged per-step scalars [3][ROWS][tile + 1]
   template <int ROWS, int BLOCK, int TILE, class Lay>
   __device__ __forceinline__ void stage(const Lay& lay, int64_t row0, int, int ts, int te,
                                         unsigned char* sm) const {
@@ -540,20 +605,22 @@ struct RetraceEst {
     constexpr int SROW = TILE + 1;  // tile + 1 steps per row
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float* raw_q = reinterpret_cast<float*>(sm) + warp * 64 * st.A;
-    float* raw_p = raw_q + 32 * st.A;
-    float* s_ev = reinterpret_cast<float*>(sm) + NW * 64 * st.A;
+    float* raw = reinterpret_cast<float*>(sm) + warp * retrace_raw_floats(st.A, false);
+    float* s_ev = reinterpret_cast<float*>(sm) + NW * retrace_raw_floats(st.A, false);
     float* s_qa = s_ev + ROWS * SROW;
     float* s_c = s_qa + ROWS * SROW;
     const int nst = te - ts + (te < b.T ? 1 : 0);
     const int per_row = (nst + 31) / 32;
-    for (int ch = warp; ch < ROWS * per_row; ch += NW) {
-      const int rr = ch / per_row, m = ch - rr * per_row;
-      if (row0 + rr >= lay.E) continue;
-      const int i0 = m * 32;
-      st.chunk(lay.at(row0 + rr, ts + i0), min(32, nst - i0), lane, raw_q, raw_p, s_ev, s_qa, s_c,
-               rr * SROW + i0 + lane);
-    }
+    st.template walk<retrace_bufs(false)>(ROWS * per_row, warp, NW, lane, raw, s_ev, s_qa, s_c,
+            [&](int ch, int64_t* e0, int* cnt, int* slot) {
+              const int rr = ch / per_row, m = ch - rr * per_row;
+              if (row0 + rr >= lay.E) return false;
+              const int i0 = m * 32;
+              *e0 = lay.at(row0 + rr, ts + i0);
+              *cnt = min(32, nst - i0);
+              *slot = rr * SROW + i0 + lane;
+              return true;
+            });
     __syncthreads();
   }
   // time-major: one chunk = one step of 32 consecutive environments;
@@ -564,15 +631,18 @@ struct RetraceEst {
     constexpr int SROWS = (BLOCK / 32) * 8 + 1;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float* raw_q = reinterpret_cast<float*>(sm) + warp * 64 * st.A;
-    float* raw_p = raw_q + 32 * st.A;
-    float* s_ev = reinterpret_cast<float*>(sm) + NW * 64 * st.A;
+    float* raw = reinterpret_cast<float*>(sm) + warp * retrace_raw_floats(st.A, true);
+    float* s_ev = reinterpret_cast<float*>(sm) + NW * retrace_raw_floats(st.A, true);
     float* s_qa = s_ev + SROWS * 32;
     float* s_c = s_qa + SROWS * 32;
     const int nst = te - ts + (te < b.T ? 1 : 0);
     const int cnt = (int)min((int64_t)32, lay.E - row0);
-    for (int i = warp; i < nst; i += NW)
-      st.chunk(lay.at(row0, ts + i), cnt, lane, raw_q, raw_p, s_ev, s_qa, s_c, i * 32 + lane);
+    st.template walk<retrace_bufs(true)>(nst, warp, NW, lane, raw, s_ev, s_qa, s_c, [&](int i, int64_t* e0, int* c, int* slot) {
+      *e0 = lay.at(row0, ts + i);
+      *c = cnt;
+      *slot = i * 32 + lane;
+      return true;
+    });
     __syncthreads();
   }
 
@@ -584,7 +654,7 @@ struct RetraceEst {
     constexpr bool kTM = IO::kTimeMajor;
     const int t0 = io.t0, n = io.n;
     const int NW = blockDim.x >> 5;
-    const float* s_ev = reinterpret_cast<const float*>(sm) + NW * 64 * st.A;
+    const float* s_ev = reinterpret_cast<const float*>(sm) + NW * retrace_raw_floats(st.A, kTM);
     const int srows = tile + 1;
     const int plane = srows * nrows;
     const float* s_qa = s_ev + plane;
