@@ -24,6 +24,7 @@ RLCA_MULTIPASS = 0x2
 RLCA_PSUM_EXCLUSIVE = 0x4
 RLCA_PSUM_FLAG_IS_START = 0x8
 RLCA_INPUTS_READY = 0x10
+RLCA_BF16 = 0x20
 
 RLCA_EST_GAE = 1
 RLCA_EST_DISCOUNTED_RETURN = 2

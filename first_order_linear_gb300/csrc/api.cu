@@ -86,6 +86,20 @@ int check_sizes(int64_t E, int64_t T, int* status) {
 bool flags_ok(uint32_t flags, uint32_t allowed) { return (flags & ~allowed) == 0u; }
 
 constexpr uint32_t kLayoutFlags = RLCA_TIME_MAJOR | RLCA_MULTIPASS | RLCA_INPUTS_READY;
+// flags of the calls whose float arrays may be bfloat16
+constexpr uint32_t kFloatFlags = kLayoutFlags | RLCA_BF16;
+
+template <class T>
+struct TypeTag {
+  using type = T;
+};
+// f(TypeTag<ST>{}) with ST the element type of the call's float arrays
+template <class F>
+int with_storage(uint32_t flags, F&& f) {
+  return (flags & RLCA_BF16) ? f(TypeTag<bf16>{}) : f(TypeTag<float>{});
+}
+// bytes of one float-array element
+size_t fbytes(uint32_t flags) { return (flags & RLCA_BF16) ? 2 : 4; }
 
 template <class Est>
 int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flags, void* ws, size_t ws_bytes,
@@ -114,7 +128,8 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const bool retrace = kind == Kind::Retrace;
   Plan q = {};
   q.time_major = (flags & RLCA_TIME_MAJOR) != 0;
-  q.staged = kStagedPath && vec && !q.time_major && !retrace && T % 4 == 0;
+  const bool bf16_io = (flags & RLCA_BF16) != 0;
+  q.staged = kStagedPath && vec && !q.time_major && !retrace && !bf16_io && T % 4 == 0;
   if (q.staged) {
     int W = (int)std::min<int64_t>(next_pow2((T + kEsSteps - 1) / kEsSteps), kEsMaxWidth);
     if (flags & RLCA_MULTIPASS) W = std::max(1, W / 4);
@@ -208,11 +223,12 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const bool tf_few = q.nseg > 1 && tf_threads < (int64_t)sm_count * 128 && T > 4 * 8 * tf_ct;
   if (q.time_major && !retrace && !tf_few && T % 8 == 0 && !(flags & RLCA_MULTIPASS) &&
       (uint64_t)E * (uint64_t)T < (uint64_t{1} << 32)) {
-    // staged: 16-byte pieces of 128-byte step rows (32 environments, E % 4
-    // == 0, aligned inputs) through a ring of 64-step tiles.  With 8
+    // staged: 16-byte pieces of the step rows of 32 environments (E a
+    // multiple of the environments per piece, aligned inputs) through a ring
+    // of 64-step tiles.  With 8
     // environments per CTA the rows are single 32-byte sectors and reading
     // them straight into registers is faster.
-    const bool staged = kTmStaged && vec && E % 4 == 0 && tf_ew == 32;
+    const bool staged = kTmStaged && vec && E % (bf16_io ? 8 : 4) == 0 && tf_ew == 32;
     const int EW = tf_ew, CT = staged ? std::min(tf_ct, tf_ew == 32 ? 8 : 32) : tf_ct;
     q.tm_fast = true;
     q.tm_staged = staged;
@@ -273,7 +289,7 @@ int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions
     default: return RLCA_ERR_INVALID_ARG;
   }
   const uint32_t allowed =
-      kLayoutFlags | (kind == Kind::PrefixSum ? (RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START) : 0u);
+      kFloatFlags | (kind == Kind::PrefixSum ? (RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START) : 0u);
   if (!flags_ok(flags, allowed)) return RLCA_ERR_INVALID_ARG;
   if (kind == Kind::Retrace && num_actions < 1) return RLCA_ERR_INVALID_ARG;
   if (kind == Kind::Retrace && num_actions > RLCA_MAX_ACTIONS) return RLCA_ERR_UNSUPPORTED;
@@ -284,8 +300,8 @@ int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions
   // the call picks the staged or the direct path from its pointers' alignment,
   // which the query cannot see: report the larger of the two needs
   Plan pd, ps;
-  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, false, &pd)) return RLCA_ERR_INVALID_ARG;
-  if (!make_plan(kind, E, (int)T, num_actions, flags & kLayoutFlags, sm, true, &ps)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kFloatFlags, sm, false, &pd)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kFloatFlags, sm, true, &ps)) return RLCA_ERR_INVALID_ARG;
   *bytes = std::max(pd.ws_bytes, ps.ws_bytes);
   return RLCA_OK;
 }
@@ -296,24 +312,31 @@ int rlca_gae(const float* rewards, const float* values, const uint8_t* terminate
              rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !values || !advantages || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T);
   if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
-                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                   {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{advantages, nf}, {returns, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) &&
                    aligned(returns, 16) && aligned(terminated, 4) && aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  if (truncated) {
-    GaeEst<true> e;
-    e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma; e.gl = gamma * lambda;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    auto fill = [&](auto& e) {
+      e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma;
+      e.gl = gamma * lambda;
+    };
+    if (truncated) {
+      GaeEst<true, ST> e;
+      fill(e);
+      return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    GaeEst<false, ST> e;
+    fill(e);
     return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  GaeEst<false> e;
-  e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.gamma = gamma; e.gl = gamma * lambda;
-  return launch(Kind::Gae, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_value_targets(const float* rewards, const float* values, const uint8_t* terminated,
@@ -323,30 +346,33 @@ int rlca_value_targets(const float* rewards, const float* values, const uint8_t*
                        rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !values || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
   if (!advantages && !returns && !disc_returns && !td_lambda_returns) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T);
   if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
-                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                   {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{advantages, nf}, {returns, nf}, {disc_returns, nf}, {td_lambda_returns, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(advantages, 16) &&
                    aligned(returns, 16) && aligned(disc_returns, 16) && aligned(td_lambda_returns, 16) &&
                    aligned(terminated, 4) && aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  auto fill = [&](auto& e) {
-    e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.disc = disc_returns;
-    e.td = td_lambda_returns; e.gamma = gamma; e.gl = gamma * lambda;
-  };
-  if (truncated) {
-    ValueTargetsEst<true> e;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    auto fill = [&](auto& e) {
+      e.b = b; e.r = rewards; e.v = values; e.adv = advantages; e.ret = returns; e.disc = disc_returns;
+      e.td = td_lambda_returns; e.gamma = gamma; e.gl = gamma * lambda;
+    };
+    if (truncated) {
+      ValueTargetsEst<true, ST> e;
+      fill(e);
+      return launch(Kind::ValueTargets, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    ValueTargetsEst<false, ST> e;
     fill(e);
     return launch(Kind::ValueTargets, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  ValueTargetsEst<false> e;
-  fill(e);
-  return launch(Kind::ValueTargets, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_discounted_return(const float* rewards, const uint8_t* terminated, const uint8_t* truncated,
@@ -355,23 +381,26 @@ int rlca_discounted_return(const float* rewards, const uint8_t* terminated, cons
                            rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !returns || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T);
   if (any_overlap({{rewards, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
-                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                   {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{returns, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(returns, 16) && aligned(terminated, 4) && aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  if (truncated) {
-    DiscEst<true> e;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    if (truncated) {
+      DiscEst<true, ST> e;
+      e.b = b; e.r = rewards; e.out = returns; e.gamma = gamma;
+      return launch(Kind::Disc, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    DiscEst<false, ST> e;
     e.b = b; e.r = rewards; e.out = returns; e.gamma = gamma;
     return launch(Kind::Disc, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  DiscEst<false> e;
-  e.b = b; e.r = rewards; e.out = returns; e.gamma = gamma;
-  return launch(Kind::Disc, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_td_lambda(const float* rewards, const float* values, const uint8_t* terminated, const uint8_t* truncated,
@@ -380,26 +409,31 @@ int rlca_td_lambda(const float* rewards, const float* values, const uint8_t* ter
                    rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !values || !returns || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T);
   if (any_overlap({{rewards, nf}, {values, nf}, {terminated, nb}, {truncated, nb}, {trunc_value, nf},
-                   {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                   {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{returns, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(returns, 16) && aligned(terminated, 4) &&
                    aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  if (truncated) {
-    TdLambdaEst<true> e;
-    e.b = b; e.r = rewards; e.v = values; e.out = returns; e.gamma = gamma; e.gl = gamma * lambda;
-    e.one_minus_lambda = 1.f - lambda;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    auto fill = [&](auto& e) {
+      e.b = b; e.r = rewards; e.v = values; e.out = returns; e.gamma = gamma; e.gl = gamma * lambda;
+      e.one_minus_lambda = 1.f - lambda;
+    };
+    if (truncated) {
+      TdLambdaEst<true, ST> e;
+      fill(e);
+      return launch(Kind::TdLambda, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    TdLambdaEst<false, ST> e;
+    fill(e);
     return launch(Kind::TdLambda, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  TdLambdaEst<false> e;
-  e.b = b; e.r = rewards; e.v = values; e.out = returns; e.gamma = gamma; e.gl = gamma * lambda;
-  e.one_minus_lambda = 1.f - lambda;
-  return launch(Kind::TdLambda, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_vtrace(const float* rewards, const float* values, const float* logp_target, const float* logp_behaviour,
@@ -409,28 +443,33 @@ int rlca_vtrace(const float* rewards, const float* values, const float* logp_tar
                 rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !values || !logp_target || !logp_behaviour || !vs || (truncated && !trunc_value))
     return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T);
   if (any_overlap({{rewards, nf}, {values, nf}, {logp_target, nf}, {logp_behaviour, nf}, {terminated, nb},
-                   {truncated, nb}, {trunc_value, nf}, {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+                   {truncated, nb}, {trunc_value, nf}, {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{vs, nf}, {pg_advantages, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(values, 16) && aligned(logp_target, 16) &&
                    aligned(logp_behaviour, 16) && aligned(vs, 16) && aligned(pg_advantages, 16) &&
                    aligned(terminated, 4) && aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  if (truncated) {
-    VtraceEst<true> e;
-    e.b = b; e.r = rewards; e.v = values; e.lpt = logp_target; e.lpb = logp_behaviour; e.vs = vs;
-    e.pg = pg_advantages; e.gamma = gamma; e.rho_bar = rho_bar; e.c_bar = c_bar; e.lambda = lambda;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    auto fill = [&](auto& e) {
+      e.b = b; e.r = rewards; e.v = values; e.lpt = logp_target; e.lpb = logp_behaviour; e.vs = vs;
+      e.pg = pg_advantages; e.gamma = gamma; e.rho_bar = rho_bar; e.c_bar = c_bar; e.lambda = lambda;
+    };
+    if (truncated) {
+      VtraceEst<true, ST> e;
+      fill(e);
+      return launch(Kind::Vtrace, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    VtraceEst<false, ST> e;
+    fill(e);
     return launch(Kind::Vtrace, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  VtraceEst<false> e;
-  e.b = b; e.r = rewards; e.v = values; e.lpt = logp_target; e.lpb = logp_behaviour; e.vs = vs;
-  e.pg = pg_advantages; e.gamma = gamma; e.rho_bar = rho_bar; e.c_bar = c_bar; e.lambda = lambda;
-  return launch(Kind::Vtrace, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_retrace(const float* q, const float* pi, const float* mu_a, const int32_t* actions, const float* rewards,
@@ -439,7 +478,8 @@ int rlca_retrace(const float* q, const float* pi, const float* mu_a, const int32
                  float lambda, uint32_t flags, void* workspace, size_t workspace_bytes, rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
+  if (flags & RLCA_BF16) return RLCA_ERR_UNSUPPORTED;
   if (num_actions < 1) return RLCA_ERR_INVALID_ARG;
   if (num_actions > RLCA_MAX_ACTIONS) return RLCA_ERR_UNSUPPORTED;
   if (!q || !pi || !mu_a || !actions || !rewards || !q_ret || (truncated && !trunc_value))
@@ -467,15 +507,18 @@ int rlca_elig_trace(const float* x, const uint8_t* terminated, const uint8_t* tr
                     rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!x || !out) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t nf = (size_t)(E * T) * fbytes(flags), nb = (size_t)(E * T);
   if (any_overlap({{x, nf}, {terminated, nb}, {truncated, nb}, {workspace, workspace_bytes}}, {{out, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(x, 16) && aligned(out, 16) && aligned(terminated, 4) && aligned(truncated, 4);
-  EligEst e;
-  e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.gl = gamma * lambda;
-  return launch(Kind::Elig, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    EligEst<ST> e;
+    e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.gl = gamma * lambda;
+    return launch(Kind::Elig, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_episodic_prefix_sum(const void* x, int dtype, const uint8_t* terminated, const uint8_t* truncated,
@@ -483,14 +526,15 @@ int rlca_episodic_prefix_sum(const void* x, int dtype, const uint8_t* terminated
                              size_t workspace_bytes, rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags | RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags | RLCA_PSUM_EXCLUSIVE | RLCA_PSUM_FLAG_IS_START)) return RLCA_ERR_INVALID_ARG;
   if (dtype != RLCA_F32 && dtype != RLCA_I32) return RLCA_ERR_INVALID_ARG;
+  if (dtype == RLCA_I32 && (flags & RLCA_BF16)) return RLCA_ERR_INVALID_ARG;
   if (!x || !out) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);
+  const size_t nf = (size_t)(E * T) * fbytes(flags), nb = (size_t)(E * T);
   if (any_overlap({{x, nf}, {terminated, nb}, {truncated, nb}, {workspace, workspace_bytes}}, {{out, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(x, 16) && aligned(out, 16) && aligned(terminated, 4) && aligned(truncated, 4);
-  const uint32_t core = flags & kLayoutFlags;
+  const uint32_t core = flags & kFloatFlags;
   const int excl = (flags & RLCA_PSUM_EXCLUSIVE) ? 1 : 0;
   const int start = (flags & RLCA_PSUM_FLAG_IS_START) ? 1 : 0;
   if (dtype == RLCA_I32) {
@@ -498,29 +542,35 @@ int rlca_episodic_prefix_sum(const void* x, int dtype, const uint8_t* terminated
     e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.exclusive = excl; e.flag_is_start = start;
     return launch(Kind::PrefixSum, e, E, T, 0, core, workspace, workspace_bytes, vec, stream);
   }
-  PrefixSumEst<float> e;
-  e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.exclusive = excl; e.flag_is_start = start;
-  return launch(Kind::PrefixSum, e, E, T, 0, core, workspace, workspace_bytes, vec, stream);
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    PrefixSumEst<float, ST> e;
+    e.x = x; e.term = terminated; e.trunc = truncated; e.out = out; e.exclusive = excl; e.flag_is_start = start;
+    return launch(Kind::PrefixSum, e, E, T, 0, core, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_affine_scan(const float* alpha, const float* beta, const float* carry, float* out, int64_t E, int64_t T,
                      int reverse, uint32_t flags, void* workspace, size_t workspace_bytes, rlca_stream_t stream) {
   int st;
   if (check_sizes(E, T, &st)) return st;
-  if (!flags_ok(flags, kLayoutFlags)) return RLCA_ERR_INVALID_ARG;
+  if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
   if (!alpha || !beta || !out) return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4;
-  if (any_overlap({{alpha, nf}, {beta, nf}, {carry, (size_t)E * 4}, {workspace, workspace_bytes}}, {{out, nf}}))
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe;
+  if (any_overlap({{alpha, nf}, {beta, nf}, {carry, (size_t)E * fe}, {workspace, workspace_bytes}}, {{out, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(alpha, 16) && aligned(beta, 16) && aligned(out, 16);
-  if (reverse) {
-    AffineEst<true> e;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    if (reverse) {
+      AffineEst<true, ST> e;
+      e.alpha = alpha; e.beta = beta; e.carry = carry; e.out = out;
+      return launch(Kind::Affine, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+    }
+    AffineEst<false, ST> e;
     e.alpha = alpha; e.beta = beta; e.carry = carry; e.out = out;
     return launch(Kind::Affine, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
-  }
-  AffineEst<false> e;
-  e.alpha = alpha; e.beta = beta; e.carry = carry; e.out = out;
-  return launch(Kind::Affine, e, E, T, 0, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 }  // extern "C"

@@ -140,7 +140,8 @@ static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, c
 
 template <class Est, int W>
 static cudaError_t launch_es_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
-  if constexpr (kStagedPath && Est::kStageable && W <= kEsMaxWidth) {
+  if constexpr (kStagedPath && Est::kStageable && W <= kEsMaxWidth &&
+                std::is_same<typename Est::Store, float>::value) {
     return launch_one<Est>(es_scan_kernel<Est, W>, p, es_smem_bytes<Est, W>(), est, g, s);
   } else {
     return cudaErrorInvalidConfiguration;

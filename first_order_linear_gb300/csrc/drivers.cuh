@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
 
     est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, ts, te, est_smem);
     typename Est::template Regs<L> R;
-    const GIO<EnvMajor> io{lay, row, t0, n, vec};
+    const GIO<EnvMajor, false, typename Est::Store> io{lay, row, t0, n, vec};
     est.template load<L>(R, io, rloc, ts, S::TILE, S::ROWS, est_smem);
     if (it == ntiles - 1) pdl_trigger();
 
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
 
   est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, 0, g.T, est_smem);
   typename Est::template Regs<L> R;
-  const GIO<EnvMajor, true> io{lay, row, t0, n, true};
+  const GIO<EnvMajor, true, typename Est::Store> io{lay, row, t0, n, true};
   est.template load<L>(R, io, rloc, 0, S::TILE, S::ROWS, est_smem);
   pdl_trigger();
 
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 
     est.template stage_tm<S::BLOCK>(lay, row0, ts, te, est_smem);
     typename Est::template Regs<L> R;
-    const GIO<TimeMajor> io{lay, row, t0, n, false};
+    const GIO<TimeMajor, false, typename Est::Store> io{lay, row, t0, n, false};
     est.template load<L>(R, io, lane, ts, S::TILE, 32, est_smem);
     if (it == ntiles - 1) pdl_trigger();
     if constexpr (Est::kNb > 0) {
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK)
     const int ts = tile * S::TILE;
     const int t0 = ts + c * L;
     const int n = (row_ok && t0 < g.T) ? L : 0;
-    const TmIO32 io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32};
+    const TmIO32<typename Est::Store> io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32};
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
@@ -524,11 +524,17 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK)
   using S = TsShape<EW, CT>;
   using V = typename Est::V;
   constexpr bool BWD = Est::kBackward;
+  using ST = typename Est::Store;
   constexpr int L = S::L, PAD = S::PAD, NS = S::NS, CS = S::CS, FB = S::FB;
-  constexpr int QR = EW / 4;            // 4-element pieces per step row
-  constexpr int PIECES = S::TILE * QR;  // pieces per staged input and tile
+  constexpr int ES = (int)sizeof(ST);
+  constexpr int FPE = 16 / ES;              // environments per 16-byte piece of a float row
+  constexpr int QF = EW / FPE;              // float pieces per step row
+  constexpr int QB = EW / 4;                // 4-byte flag pieces per step row
+  constexpr int PF = S::TILE * QF;          // float pieces per staged input and tile
+  constexpr int PB = S::TILE * QB;          // flag pieces per staged input and tile
   constexpr size_t STAGE = ts_stage_bytes<Est, EW, CT>();
-  static_assert(PIECES % S::BLOCK == 0, "whole copy rounds");
+  constexpr size_t FLAGS_AT = (size_t)ES * Est::kSF * FB;  // flag buffers' offset in a stage
+  static_assert(PF % S::BLOCK == 0 && PB % S::BLOCK == 0, "whole copy rounds");
 
   extern __shared__ __align__(16) unsigned char smem[];
   Aff<V>* xs = reinterpret_cast<Aff<V>*>(smem);  // [CT][PAD] chunk maps
@@ -557,21 +563,35 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK)
     if (it < ntiles) {
       const int ts = (BWD ? ntiles - 1 - it : it) * S::TILE;
       unsigned char* st = ring + (size_t)(it % NS) * STAGE;
+      // float inputs: 16-byte pieces of FPE environments (E % FPE == 0: a
+      // piece is wholly inside or outside the rows)
 #pragma unroll
-      for (int i = 0; i < PIECES / S::BLOCK; ++i) {
+      for (int i = 0; i < PF / S::BLOCK; ++i) {
         const int p = tid + i * S::BLOCK;
-        const int r = p / QR, q = p % QR;
+        const int r = p / QF, q = p % QF;
+        const int t = ts + r;
+        const uint32_t e = e0 + (uint32_t)(FPE * q);
+        if (t < g.T && e < E32) {
+          const uint32_t go = (uint32_t)t * E32 + e;
+          const int so = (r / L) * CS + (r % L) * EW + FPE * q;
+#pragma unroll
+          for (int b = 0; b < Est::kSF; ++b)
+            cp_async16(reinterpret_cast<ST*>(st) + b * FB + so, static_cast<const ST*>(in.fin[b]) + go);
+        }
+      }
+      // flag inputs: 4-byte pieces of 4 environments
+#pragma unroll
+      for (int i = 0; i < PB / S::BLOCK; ++i) {
+        const int p = tid + i * S::BLOCK;
+        const int r = p / QB, q = p % QB;
         const int t = ts + r;
         const uint32_t e = e0 + 4u * (uint32_t)q;
-        if (t < g.T && e < E32) {  // E % 4 == 0: a piece is wholly inside or outside
+        if (t < g.T && e < E32) {
           const uint32_t go = (uint32_t)t * E32 + e;
           const int so = (r / L) * CS + (r % L) * EW + 4 * q;
 #pragma unroll
-          for (int b = 0; b < Est::kSF; ++b)
-            cp_async16(reinterpret_cast<float*>(st) + b * FB + so, static_cast<const float*>(in.fin[b]) + go);
-#pragma unroll
           for (int b = 0; b < Est::kSB; ++b)
-            if (in.bin[b] != nullptr) cp_async4(st + (size_t)4 * Est::kSF * FB + b * FB + so, in.bin[b] + go);
+            if (in.bin[b] != nullptr) cp_async4(st + FLAGS_AT + b * FB + so, in.bin[b] + go);
         }
       }
     }
@@ -608,7 +628,7 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK)
     const int t0 = ts + c * L;
     const int n = (row_ok && t0 < g.T) ? L : 0;
     const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
-    const TmSIO<EW, FB> io{reinterpret_cast<const float*>(st), st + (size_t)4 * Est::kSF * FB, c * CS + j, row, t0, n,
+    const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
                            (uint32_t)t0 * E32 + (uint32_t)row, E32};
 
     typename Est::template Regs<L> R;

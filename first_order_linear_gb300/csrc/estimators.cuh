@@ -59,7 +59,7 @@ struct BoundaryRegs {
 };
 
 // flags are staged byte inputs 0 (terminated) and 1 (truncated)
-template <bool HAS_TRUNC, int L, class IO>
+template <bool HAS_TRUNC, class ST, int L, class IO>
 __device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryRegs<L>& R, const IO& io) {
   R.term = io.template flags<L>(0, b.term);
   R.trunc = HAS_TRUNC ? (io.template flags<L>(1, b.trunc) & ~R.term) : 0u;
@@ -68,9 +68,9 @@ __device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryReg
   if (HAS_TRUNC && R.trunc != 0u) {  // truncations are rare: one branch instead of L predicated loads
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if ((R.trunc >> k) & 1u) R.tv[k] = __ldg(b.tv + io.at(k));
+      if ((R.trunc >> k) & 1u) R.tv[k] = Stor<ST>::ld(b.tv, io.at(k));
   }
-  R.boot = (io.n > 0 && io.t0 + io.n == b.T && b.boot != nullptr) ? __ldg(b.boot + io.row) : 0.f;
+  R.boot = (io.n > 0 && io.t0 + io.n == b.T && b.boot != nullptr) ? Stor<ST>::ld(b.boot, io.row) : 0.f;
 }
 
 template <class F>
@@ -99,8 +99,9 @@ __device__ __forceinline__ bool cut(const BoundaryRegs<L>& R, int k) {
 //   beta_t  = gamma lambda (1 - d_t) [t < T-1],    carry 0
 //   outputs adv_t = A_t, ret_t = A_t + V_t
 // ===========================================================================
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct GaeEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
@@ -132,14 +133,14 @@ struct GaeEst : NoStage {
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     io.template f<L>(0, r, R.r);
     io.template f<L>(1, v, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
   template <class Lay>
   __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
-    g[0] = __ldg(v + lay.at(row, t));
+    g[0] = Stor<ST>::ld(v, lay.at(row, t));
   }
   template <int L>
   __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
@@ -167,8 +168,9 @@ struct GaeEst : NoStage {
 //   alpha_t = r_t + gamma trunc_t trunc_value_t,  beta_t = gamma (1 - d_t),
 //   carry A_T = bootstrap
 // ===========================================================================
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct DiscEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
@@ -191,12 +193,12 @@ struct DiscEst : NoStage {
     float r[L], o[L];
   };
   __device__ __forceinline__ float row_carry(int64_t row) const {
-    return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
+    return b.boot != nullptr ? Stor<ST>::ld(b.boot, row) : 0.f;
   }
   template <int L, class IO>
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     io.template f<L>(0, r, R.r);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>&, float*) const {}
@@ -225,8 +227,9 @@ struct DiscEst : NoStage {
 //   alpha_t = r_t + gamma [trunc_t tv_t + (1 - d_t)(1 - lambda) V_next(t)]
 //   beta_t  = gamma lambda (1 - d_t),   carry A_T = bootstrap
 // ===========================================================================
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct TdLambdaEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
@@ -251,20 +254,20 @@ struct TdLambdaEst : NoStage {
     float r[L], v[L], vnext, o[L];
   };
   __device__ __forceinline__ float row_carry(int64_t row) const {
-    return b.boot != nullptr ? __ldg(b.boot + row) : 0.f;
+    return b.boot != nullptr ? Stor<ST>::ld(b.boot, row) : 0.f;
   }
   template <int L, class IO>
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     io.template f<L>(0, r, R.r);
     io.template f<L>(1, v, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
   template <class Lay>
   __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
-    g[0] = __ldg(v + lay.at(row, t));
+    g[0] = Stor<ST>::ld(v, lay.at(row, t));
   }
   template <int L>
   __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
@@ -296,8 +299,9 @@ struct TdLambdaEst : NoStage {
 // termination: r; truncation: r + gamma tv; window edge: r + gamma b), so
 // it needs no third scan.
 // ===========================================================================
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct ValueTargetsEst : NoStage {
+  using Store = ST;
   using V = F2;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
@@ -329,20 +333,20 @@ struct ValueTargetsEst : NoStage {
     float oa[L], od[L];
   };
   __device__ __forceinline__ F2 row_carry(int64_t row) const {
-    return F2(0.f, b.boot != nullptr ? __ldg(b.boot + row) : 0.f);
+    return F2(0.f, b.boot != nullptr ? Stor<ST>::ld(b.boot, row) : 0.f);
   }
   template <int L, class IO>
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
     io.template f<L>(0, r, R.r);
     io.template f<L>(1, v, R.v);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
     R.vnext = 0.f;
   }
   template <int L>
   __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
   template <class Lay>
   __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
-    g[0] = __ldg(v + lay.at(row, t));
+    g[0] = Stor<ST>::ld(v, lay.at(row, t));
   }
   template <int L>
   __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
@@ -379,8 +383,9 @@ struct ValueTargetsEst : NoStage {
 //   beta_t  = gamma c_t (1 - d_t) [t < T-1],   carry 0
 //   vs_t = V_t + A_t;  pg_t = rho_t (r_t + gamma vs_next(t) - V_t)
 // ===========================================================================
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct VtraceEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
@@ -420,7 +425,7 @@ struct VtraceEst : NoStage {
     io.template f<L>(1, v, R.v);
     io.template f<L>(2, lpt, a);
     io.template f<L>(3, lpb, bb);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
 #pragma unroll
     for (int k = 0; k < L; ++k) {
       const float ratio = expf(a[k] - bb[k]);
@@ -434,7 +439,7 @@ struct VtraceEst : NoStage {
   __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const { g[0] = R.v[0]; }
   template <class Lay>
   __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
-    g[0] = __ldg(v + lay.at(row, t));
+    g[0] = Stor<ST>::ld(v, lay.at(row, t));
   }
   template <int L>
   __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const { R.vnext = g[0]; }
@@ -578,6 +583,7 @@ struct RetraceStage {
 
 template <bool HAS_TRUNC>
 struct RetraceEst {
+  using Store = float;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
@@ -650,7 +656,7 @@ struct RetraceEst {
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int slot, int ts, int tile, int nrows,
                                        unsigned char* sm) const {
     io.template f<L>(0, r, R.r);
-    load_boundary<HAS_TRUNC, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, float, L>(b, R.bd, io);
     constexpr bool kTM = IO::kTimeMajor;
     const int t0 = io.t0, n = io.n;
     const int NW = blockDim.x >> 5;
@@ -704,7 +710,9 @@ struct RetraceEst {
 // Eligibility trace, forward (rl-triton §1, §5)
 //   alpha_t = x_t,  beta_t = gamma lambda (1 - d_{t-1}),  e_{-1} = 0
 // ===========================================================================
+template <class ST = float>
 struct EligEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
@@ -769,8 +777,9 @@ struct EligEst : NoStage {
 // int32 runs in uint32 arithmetic (wraps modulo 2^32; beta is 0 or 1, so any
 // grouping gives the same bits).
 // ===========================================================================
-template <class VT>
+template <class VT, class ST = float>
 struct PrefixSumEst : NoStage {
+  using Store = ST;
   using V = VT;
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
@@ -843,8 +852,9 @@ struct PrefixSumEst : NoStage {
 // ===========================================================================
 // Generic affine scan over precomputed coefficients (rl-triton §4)
 // ===========================================================================
-template <bool BWD>
+template <bool BWD, class ST = float>
 struct AffineEst : NoStage {
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = BWD;
   static constexpr int kNb = 0;
@@ -866,7 +876,7 @@ struct AffineEst : NoStage {
     float a[L], b[L], o[L];
   };
   __device__ __forceinline__ float row_carry(int64_t row) const {
-    return carry != nullptr ? __ldg(carry + row) : 0.f;
+    return carry != nullptr ? Stor<ST>::ld(carry, row) : 0.f;
   }
   template <int L, class IO>
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {

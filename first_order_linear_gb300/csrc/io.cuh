@@ -16,8 +16,8 @@
 namespace rlca {
 
 // VEC_CT: the vector path is known at compile time (fast driver); otherwise
-// `vec` decides at run time
-template <class Lay, bool VEC_CT = false>
+// `vec` decides at run time.  ST: element type of the float arrays.
+template <class Lay, bool VEC_CT = false, class ST = float>
 struct GIO {
   static constexpr bool kTimeMajor = Lay::kTimeMajor;
   const Lay& lay;
@@ -30,7 +30,7 @@ struct GIO {
   __device__ __forceinline__ int64_t at(int k) const { return lay.at(row, t0 + k); }
   template <int L>
   __device__ __forceinline__ void f(int, const float* p, float (&o)[L]) const {
-    load_vals<L>(p, lay, row, t0, n, vec(), o);
+    load_vals<L, Lay, ST>(p, lay, row, t0, n, vec(), o);
   }
   template <int L>
   __device__ __forceinline__ void i(int, const int32_t* p, uint32_t (&o)[L]) const {
@@ -42,7 +42,7 @@ struct GIO {
   }
   template <int L>
   __device__ __forceinline__ void put(int, float* p, const float (&v)[L]) const {
-    if (p != nullptr) store_vals<L>(p, lay, row, t0, n, vec(), v);
+    if (p != nullptr) store_vals<L, Lay, ST>(p, lay, row, t0, n, vec(), v);
   }
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* p, const uint32_t (&v)[L]) const {
@@ -54,6 +54,7 @@ struct GIO {
 // steps are either all in range (n == L) or none (n == 0), and every array's
 // element (t0 + k, row) sits at element offset off + k * E, computed in 32
 // bits (the planner takes this path only when E * T < 2^32).
+template <class ST = float>
 struct TmIO32 {
   static constexpr bool kTimeMajor = true;
   int64_t row;
@@ -67,7 +68,7 @@ struct TmIO32 {
   template <int L>
   __device__ __forceinline__ void f(int, const float* __restrict__ p, float (&v)[L]) const {
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? __ldg(p + o(k)) : 0.f;
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? Stor<ST>::ld(p, o(k)) : 0.f;
   }
   template <int L>
   __device__ __forceinline__ void i(int, const int32_t* __restrict__ p, uint32_t (&v)[L]) const {
@@ -86,7 +87,7 @@ struct TmIO32 {
   __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) p[o(k)] = v[k];
+    for (int k = 0; k < L; ++k) Stor<ST>::st(p, o(k), v[k]);
   }
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {
@@ -97,13 +98,14 @@ struct TmIO32 {
 };
 
 // Time-major I/O of the staged time-major driver: inputs from the current
-// shared-memory stage (float input b at fbuf + b * FB, flag input b at
-// bbuf + b * FB; the thread's step k at slot + k * EW), outputs and the rare
-// truncation-value loads straight to global memory as in TmIO32.
-template <int EW, int FB>
+// shared-memory stage (float input b at fbuf + b * FB elements of type ST,
+// flag input b at bbuf + b * FB; the thread's step k at slot + k * EW),
+// outputs and the rare truncation-value loads straight to global memory as
+// in TmIO32.
+template <int EW, int FB, class ST = float>
 struct TmSIO {
   static constexpr bool kTimeMajor = true;
-  const float* fbuf;
+  const ST* fbuf;
   const uint8_t* bbuf;
   int slot;
   int64_t row;
@@ -116,12 +118,13 @@ struct TmSIO {
   __device__ __forceinline__ int64_t at(int k) const { return (int64_t)o(k); }
   template <int L>
   __device__ __forceinline__ void f(int idx, const float*, float (&v)[L]) const {
-    const float* s = fbuf + idx * FB + slot;
+    const ST* s = fbuf + idx * FB + slot;
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? s[k * EW] : 0.f;
+    for (int k = 0; k < L; ++k) v[k] = n != 0 ? static_cast<float>(s[k * EW]) : 0.f;
   }
   template <int L>
   __device__ __forceinline__ void i(int idx, const int32_t*, uint32_t (&v)[L]) const {
+    static_assert(sizeof(ST) == 4, "int inputs are staged as 4-byte elements");
     const uint32_t* s = reinterpret_cast<const uint32_t*>(fbuf + idx * FB + slot);
 #pragma unroll
     for (int k = 0; k < L; ++k) v[k] = n != 0 ? s[k * EW] : 0u;
@@ -139,7 +142,7 @@ struct TmSIO {
   __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) p[o(k)] = v[k];
+    for (int k = 0; k < L; ++k) Stor<ST>::st(p, o(k), v[k]);
   }
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {

@@ -3,7 +3,7 @@
 #include "dispatch.cuh"
 
 namespace rlca {
-template cudaError_t run_scan<EligEst>(const EligEst&, const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<EligEst<>>(const EligEst<>&, const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<PrefixSumEst<uint32_t>>(const PrefixSumEst<uint32_t>&, const Plan&, const Geom&,
                                                       cudaStream_t);
 template cudaError_t run_scan<PrefixSumEst<float>>(const PrefixSumEst<float>&, const Plan&, const Geom&,

@@ -1,0 +1,9 @@
+// bfloat16-storage kernels of V-Trace.
+#include "dispatch.cuh"
+
+namespace rlca {
+template cudaError_t run_scan<VtraceEst<true, bf16>>(const VtraceEst<true, bf16>&,
+    const Plan&, const Geom&, cudaStream_t);
+template cudaError_t run_scan<VtraceEst<false, bf16>>(const VtraceEst<false, bf16>&,
+    const Plan&, const Geom&, cudaStream_t);
+}  // namespace rlca

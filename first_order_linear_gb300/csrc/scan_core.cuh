@@ -24,11 +24,64 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace rlca {
 
 constexpr unsigned kFullMask = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// storage of the floating-point arrays.  Arithmetic and the scan state are
+// float32 always; with RLCA_BF16 every float array of a call holds bfloat16
+// (the upper half of a float32), converted on load and rounded to nearest
+// even once on store.  An estimator's float pointers then point at elements
+// of type ST; Stor<ST> does the element access.
+// ---------------------------------------------------------------------------
+using bf16 = __nv_bfloat16;
+
+template <class ST>
+struct Stor;
+
+template <>
+struct Stor<float> {
+  static constexpr int kBytes = 4;
+  __device__ __forceinline__ static float ld(const float* p, int64_t i) { return __ldg(p + i); }
+  __device__ __forceinline__ static void st(float* p, int64_t i, float v) { p[i] = v; }
+  // four consecutive elements starting at a 16-byte boundary
+  __device__ __forceinline__ static void ld4(const float* p, int64_t i, float* o) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
+    o[0] = v.x, o[1] = v.y, o[2] = v.z, o[3] = v.w;
+  }
+  __device__ __forceinline__ static void st4(float* p, int64_t i, const float* v) {
+    *reinterpret_cast<float4*>(p + i) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+
+template <>
+struct Stor<bf16> {
+  static constexpr int kBytes = 2;
+  __device__ __forceinline__ static float from_bits(uint32_t h) { return __uint_as_float(h << 16); }
+  __device__ __forceinline__ static uint32_t to_bits(float v) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  __device__ __forceinline__ static float ld(const float* p, int64_t i) {
+    return from_bits(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
+  }
+  __device__ __forceinline__ static void st(float* p, int64_t i, float v) {
+    reinterpret_cast<unsigned short*>(p)[i] = (unsigned short)to_bits(v);
+  }
+  // four consecutive elements starting at an 8-byte boundary
+  __device__ __forceinline__ static void ld4(const float* p, int64_t i, float* o) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(p) + i));
+    o[0] = __uint_as_float(w.x << 16), o[1] = __uint_as_float(w.x & 0xffff0000u);
+    o[2] = __uint_as_float(w.y << 16), o[3] = __uint_as_float(w.y & 0xffff0000u);
+  }
+  __device__ __forceinline__ static void st4(float* p, int64_t i, const float* v) {
+    const uint2 w = make_uint2(to_bits(v[0]) | (to_bits(v[1]) << 16), to_bits(v[2]) | (to_bits(v[3]) << 16));
+    *reinterpret_cast<uint2*>(reinterpret_cast<unsigned short*>(p) + i) = w;
+  }
+};
 
 // x -> a + b * x
 template <class V>
@@ -111,22 +164,22 @@ struct TimeMajor {  // [T, E], e fastest
 // ---------------------------------------------------------------------------
 // vec: env-major rows are 16-byte aligned and T % 4 == 0, so a chunk of 4
 // steps is one float4 (one u32 of flags) and is either fully in range or not.
-template <int L, class Lay>
+template <int L, class Lay, class ST = float>
 __device__ __forceinline__ void load_vals(const float* __restrict__ p, const Lay& lay, int64_t row,
                                           int t0, int n, bool vec, float (&out)[L]) {
   if (vec) {
-    const float4* q = reinterpret_cast<const float4*>(p + lay.at(row, t0));
+    const int64_t base = lay.at(row, t0);
 #pragma unroll
     for (int i = 0; i < L / 4; ++i) {
-      float4 v = (4 * i < n) ? __ldg(q + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      out[4 * i + 0] = v.x;
-      out[4 * i + 1] = v.y;
-      out[4 * i + 2] = v.z;
-      out[4 * i + 3] = v.w;
+      if (4 * i < n) {
+        Stor<ST>::ld4(p, base + 4 * i, &out[4 * i]);
+      } else {
+        out[4 * i] = out[4 * i + 1] = out[4 * i + 2] = out[4 * i + 3] = 0.f;
+      }
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < L; ++k) out[k] = (k < n) ? __ldg(p + lay.at(row, t0 + k)) : 0.f;
+    for (int k = 0; k < L; ++k) out[k] = (k < n) ? Stor<ST>::ld(p, lay.at(row, t0 + k)) : 0.f;
   }
 }
 
@@ -179,18 +232,18 @@ __device__ __forceinline__ bool load_flag1(const uint8_t* __restrict__ p, const 
   return p != nullptr && __ldg(p + lay.at(row, t)) != 0;
 }
 
-template <int L, class Lay>
+template <int L, class Lay, class ST = float>
 __device__ __forceinline__ void store_vals(float* __restrict__ p, const Lay& lay, int64_t row, int t0,
                                            int n, bool vec, const float (&v)[L]) {
   if (vec) {
-    float4* q = reinterpret_cast<float4*>(p + lay.at(row, t0));
+    const int64_t base = lay.at(row, t0);
 #pragma unroll
     for (int i = 0; i < L / 4; ++i)
-      if (4 * i < n) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      if (4 * i < n) Stor<ST>::st4(p, base + 4 * i, &v[4 * i]);
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if (k < n) p[lay.at(row, t0 + k)] = v[k];
+      if (k < n) Stor<ST>::st(p, lay.at(row, t0 + k), v[k]);
   }
 }
 
@@ -363,7 +416,7 @@ struct TsShape : TfShape<EW, CT> {
 };
 template <class Est, int EW, int CT>
 __host__ __device__ constexpr size_t ts_stage_bytes() {
-  return align16((size_t)TsShape<EW, CT>::FB * (4 * Est::kSF + Est::kSB));
+  return align16((size_t)TsShape<EW, CT>::FB * (sizeof(typename Est::Store) * Est::kSF + Est::kSB));
 }
 template <class Est, int EW, int CT>
 __host__ __device__ constexpr size_t ts_smem_bytes() {

@@ -63,6 +63,7 @@ extern "C" int rlca_gae_static_scratch(const float* rewards, const float* values
   using namespace rlca;
   if (E < 0 || T < 0 || E > INT32_MAX || T > (int64_t(1) << 30)) return RLCA_ERR_INVALID_ARG;
   if (E == 0 || T == 0) return RLCA_OK;
+  if (flags & RLCA_BF16) return RLCA_ERR_UNSUPPORTED;
   if ((flags & ~(RLCA_TIME_MAJOR | RLCA_MULTIPASS)) != 0u) return RLCA_ERR_INVALID_ARG;
   if (!rewards || !values || !advantages || (truncated && !trunc_value)) return RLCA_ERR_INVALID_ARG;
   const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T);

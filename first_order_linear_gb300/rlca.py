@@ -9,7 +9,9 @@ Layout: env-major ``[E, T]`` by default; ``time_major=True`` takes ``[T, E]``
 (and ``[T, E, A]`` for Retrace's per-action tensors).  ``inputs_ready=True``
 sets RLCA_INPUTS_READY (the inputs were not written by the kernel just before
 this call on the stream, so the call may overlap it).  Flags may be uint8 or
-bool tensors; ``None`` means "no such flag" for the optional inputs.
+bool tensors; ``None`` means "no such flag" for the optional inputs.  Float
+tensors are float32, or all bfloat16 (RLCA_BF16: bfloat16 storage, float32
+arithmetic, outputs rounded once; not for Retrace).
 """
 from __future__ import annotations
 
@@ -52,6 +54,21 @@ _U8 = (torch.uint8, torch.bool)
 _I32 = (torch.int32,)
 
 
+def _fdt(t, name):
+    """Element type of a call's float arrays, taken from its first float
+    input: float32, or bfloat16 (RLCA_BF16: bfloat16 storage, float32
+    arithmetic).  Every other float tensor of the call must match."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"{name}: dtype {t.dtype}, expected float32 or bfloat16")
+    return t.dtype
+
+
+def _fflag(fdt):
+    return _lib.RLCA_BF16 if fdt == torch.bfloat16 else 0
+
+
 def _flags(time_major, multipass, extra=0, inputs_ready=False):
     return ((_lib.RLCA_TIME_MAJOR if time_major else 0) | (_lib.RLCA_MULTIPASS if multipass else 0)
             | (_lib.RLCA_INPUTS_READY if inputs_ready else 0) | extra)
@@ -89,11 +106,11 @@ def _stream(device, stream):
     return C.c_void_p(s.cuda_stream)
 
 
-def _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E):
+def _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F=_F):
     _check(terminated, "terminated", _U8, shape, dev, required=False)
     _check(truncated, "truncated", _U8, shape, dev, required=False)
-    _check(trunc_value, "trunc_value", _F, shape, dev, required=truncated is not None)
-    _check(bootstrap, "bootstrap", _F, (E,), dev, required=False)
+    _check(trunc_value, "trunc_value", F, shape, dev, required=truncated is not None)
+    _check(bootstrap, "bootstrap", F, (E,), dev, required=False)
 
 
 def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None, bootstrap=None, *,
@@ -104,18 +121,20 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
     False and no buffer is given."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
-    _check(rewards, "rewards", _F, shape, dev)
-    _check(values, "values", _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    _check(rewards, "rewards", F, shape, dev)
+    _check(values, "values", F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     if advantages is None:
-        advantages = torch.empty(shape, dtype=torch.float32, device=dev)
+        advantages = torch.empty(shape, dtype=fdt, device=dev)
     if returns is None and want_returns:
-        returns = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(advantages, "advantages", _F, shape, dev)
-    _check(returns, "returns", _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        returns = torch.empty(shape, dtype=fdt, device=dev)
+    _check(advantages, "advantages", F, shape, dev)
+    _check(returns, "returns", F, shape, dev, required=False)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_GAE, E, T, 0, flags, dev, workspace)
         check("rlca_gae", lib.rlca_gae(
@@ -135,18 +154,20 @@ def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_v
     disc_returns, td_lambda_returns)."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
-    _check(rewards, "rewards", _F, shape, dev)
-    _check(values, "values", _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    _check(rewards, "rewards", F, shape, dev)
+    _check(values, "values", F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     bufs = dict(advantages=advantages, returns=returns, disc_returns=disc_returns,
                 td_lambda_returns=td_lambda_returns)
     for name in bufs:
         if bufs[name] is None and name in outputs:
-            bufs[name] = torch.empty(shape, dtype=torch.float32, device=dev)
-        _check(bufs[name], name, _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+            bufs[name] = torch.empty(shape, dtype=fdt, device=dev)
+        _check(bufs[name], name, F, shape, dev, required=False)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VALUE_TARGETS, E, T, 0, flags, dev, workspace)
         check("rlca_value_targets", lib.rlca_value_targets(
@@ -162,14 +183,16 @@ def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value
     """Discounted returns G_t = r_t + gamma * G_{t+1} with the boundary rules."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
-    _check(rewards, "rewards", _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    _check(rewards, "rewards", F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        out = torch.empty(shape, dtype=fdt, device=dev)
+    _check(out, "out", F, shape, dev)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_DISCOUNTED_RETURN, E, T, 0, flags, dev, workspace)
         check("rlca_discounted_return", lib.rlca_discounted_return(
@@ -184,15 +207,17 @@ def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value
     """TD(lambda) returns."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
-    _check(rewards, "rewards", _F, shape, dev)
-    _check(values, "values", _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    _check(rewards, "rewards", F, shape, dev)
+    _check(values, "values", F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        out = torch.empty(shape, dtype=fdt, device=dev)
+    _check(out, "out", F, shape, dev)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_TD_LAMBDA, E, T, 0, flags, dev, workspace)
         check("rlca_td_lambda", lib.rlca_td_lambda(
@@ -208,19 +233,21 @@ def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, t
     """V-Trace targets and policy-gradient advantages: ``(vs, pg_advantages)``."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
     for name, t in (("rewards", rewards), ("values", values), ("logp_target", logp_target),
                     ("logp_behaviour", logp_behaviour)):
-        _check(t, name, _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+        _check(t, name, F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     if vs is None:
-        vs = torch.empty(shape, dtype=torch.float32, device=dev)
+        vs = torch.empty(shape, dtype=fdt, device=dev)
     if pg_advantages is None and want_pg:
-        pg_advantages = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(vs, "vs", _F, shape, dev)
-    _check(pg_advantages, "pg_advantages", _F, shape, dev, required=False)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        pg_advantages = torch.empty(shape, dtype=fdt, device=dev)
+    _check(vs, "vs", F, shape, dev)
+    _check(pg_advantages, "pg_advantages", F, shape, dev, required=False)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VTRACE, E, T, 0, flags, dev, workspace)
         check("rlca_vtrace", lib.rlca_vtrace(
@@ -236,21 +263,23 @@ def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None,
     """Retrace(lambda) Q targets; q and pi are [E, T, A] ([T, E, A])."""
     lib = _lib.load()
     dev = rewards.device
+    fdt = _fdt(rewards, "rewards")
+    F = (fdt,)
     E, T = _dims(rewards, time_major)
     shape = tuple(rewards.shape)
     if q.dim() != 3:
         raise ValueError("q must be 3-D")
     A = q.shape[-1]
-    _check(q, "q", _F, shape + (A,), dev)
-    _check(pi, "pi", _F, shape + (A,), dev)
-    _check(mu_a, "mu_a", _F, shape, dev)
+    _check(q, "q", F, shape + (A,), dev)
+    _check(pi, "pi", F, shape + (A,), dev)
+    _check(mu_a, "mu_a", F, shape, dev)
     _check(actions, "actions", _I32, shape, dev)
-    _check(rewards, "rewards", _F, shape, dev)
-    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E)
+    _check(rewards, "rewards", F, shape, dev)
+    _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        out = torch.empty(shape, dtype=fdt, device=dev)
+    _check(out, "out", F, shape, dev)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_RETRACE, E, T, A, flags, dev, workspace)
         check("rlca_retrace", lib.rlca_retrace(
@@ -265,15 +294,17 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
     """Accumulating eligibility trace (forward scan)."""
     lib = _lib.load()
     dev = x.device
+    fdt = _fdt(x, "x")
+    F = (fdt,)
     E, T = _dims(x, time_major)
     shape = tuple(x.shape)
-    _check(x, "x", _F, shape, dev)
+    _check(x, "x", F, shape, dev)
     _check(terminated, "terminated", _U8, shape, dev, required=False)
     _check(truncated, "truncated", _U8, shape, dev, required=False)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        out = torch.empty(shape, dtype=fdt, device=dev)
+    _check(out, "out", F, shape, dev)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_ELIG_TRACE, E, T, 0, flags, dev, workspace)
         check("rlca_elig_trace", lib.rlca_elig_trace(
@@ -284,17 +315,17 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
 
 def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=False, flag_is_start=False,
                              out=None, time_major=False, multipass=False, inputs_ready=False, workspace=None, stream=None):
-    """Per-episode running sum of x (int32 wraps; float32)."""
+    """Per-episode running sum of x (int32 wraps; float32 or bfloat16 storage)."""
     lib = _lib.load()
     dev = x.device
     E, T = _dims(x, time_major)
     shape = tuple(x.shape)
     if x.dtype == torch.int32:
         dtype = _lib.RLCA_I32
-    elif x.dtype == torch.float32:
+    elif x.dtype in (torch.float32, torch.bfloat16):
         dtype = _lib.RLCA_F32
     else:
-        raise TypeError("x must be int32 or float32")
+        raise TypeError("x must be int32, float32 or bfloat16")
     _check(x, "x", (x.dtype,), shape, dev)
     _check(terminated, "terminated", _U8, shape, dev, required=False)
     _check(truncated, "truncated", _U8, shape, dev, required=False)
@@ -302,7 +333,8 @@ def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=Fa
         out = torch.empty(shape, dtype=x.dtype, device=dev)
     _check(out, "out", (x.dtype,), shape, dev)
     extra = (_lib.RLCA_PSUM_EXCLUSIVE if exclusive else 0) | (_lib.RLCA_PSUM_FLAG_IS_START if flag_is_start else 0)
-    flags = _flags(time_major, multipass, extra, inputs_ready=inputs_ready)
+    flags = _flags(time_major, multipass, extra, inputs_ready=inputs_ready) | (
+        _lib.RLCA_BF16 if x.dtype == torch.bfloat16 else 0)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_PREFIX_SUM, E, T, 0, flags, dev, workspace)
         check("rlca_episodic_prefix_sum", lib.rlca_episodic_prefix_sum(
@@ -316,15 +348,17 @@ def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_ma
     """Generic A_t = alpha_t + beta_t * A_{t+1} (reverse) or A_{t-1} (forward)."""
     lib = _lib.load()
     dev = alpha.device
+    fdt = _fdt(alpha, "alpha")
+    F = (fdt,)
     E, T = _dims(alpha, time_major)
     shape = tuple(alpha.shape)
-    _check(alpha, "alpha", _F, shape, dev)
-    _check(beta, "beta", _F, shape, dev)
-    _check(carry, "carry", _F, (E,), dev, required=False)
+    _check(alpha, "alpha", F, shape, dev)
+    _check(beta, "beta", F, shape, dev)
+    _check(carry, "carry", F, (E,), dev, required=False)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=dev)
-    _check(out, "out", _F, shape, dev)
-    flags = _flags(time_major, multipass, inputs_ready=inputs_ready)
+        out = torch.empty(shape, dtype=fdt, device=dev)
+    _check(out, "out", F, shape, dev)
+    flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_AFFINE_SCAN, E, T, 0, flags, dev, workspace)
         check("rlca_affine_scan", lib.rlca_affine_scan(

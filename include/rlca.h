@@ -95,6 +95,19 @@ typedef struct CUstream_st *rlca_stream_t;
  * the two-pass path.  A false assertion gives wrong results (never an
  * out-of-bounds access). */
 #define RLCA_INPUTS_READY        0x10u
+/* Every floating-point array of the call -- per-step inputs and outputs and
+ * the per-environment [E] vectors (bootstrap, carry) -- holds IEEE bfloat16
+ * values (2 bytes each, the upper half of a float32) instead of float32; the
+ * pointers keep their declared float type and point at the bfloat16 data.
+ * Arithmetic and the scan state stay float32; each output is rounded to
+ * nearest-even bfloat16 once.  Flags and int32 arrays are unchanged.  With
+ * rlca_episodic_prefix_sum it applies to RLCA_F32 data only (RLCA_I32:
+ * RLCA_ERR_INVALID_ARG); rlca_retrace and rlca_gae_static_scratch return
+ * RLCA_ERR_UNSUPPORTED.  The paper defers bfloat16 I/O to future work and
+ * keeps scans in float32 (rl-triton (arXiv:2608.17641) §9 Discussion and
+ * Future Work; §4 Implementation, numerical requirements): only storage is
+ * narrowed here. */
+#define RLCA_BF16                0x20u
 /* rlca_episodic_prefix_sum: output the sum over the steps BEFORE t in t's
  * episode instead of the inclusive sum. */
 #define RLCA_PSUM_EXCLUSIVE      0x4u

@@ -20,7 +20,17 @@ TOL = 1e-4
 GAMMA, LAMBDA = 0.99, 0.95
 
 
-def assert_close(got, want, what, tol=TOL):
+# bfloat16 outputs (RLCA_BF16): the float32 result, within TOL of the
+# oracle, is rounded to nearest once.  A bfloat16 keeps 8 significant bits,
+# so rounding moves x by at most half an ulp <= 2^-8 |x|; with |x - ref| <=
+# TOL (1 + |ref|) that gives |out - ref| <= 2^-8 |ref| + TOL (1 + 2^-8) (1 + |ref|).
+BF16_REL = 2.0 ** -8
+BF16_TOL = TOL * (1.0 + 2.0 ** -8)
+
+
+def assert_close(got, want, what, tol=TOL, rel=0.0):
+    """max |got - want| <= tol (1 + |want|) + rel |want| (bit-exact for ints);
+    returns the worst |got - want| / (tol (1 + |want|) + rel |want|) * tol."""
     got = np.asarray(got)
     want = np.asarray(want)
     assert got.shape == want.shape, (what, got.shape, want.shape)
@@ -30,11 +40,12 @@ def assert_close(got, want, what, tol=TOL):
         return 0.0
     g = got.astype(np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
-    err = np.abs(g - want) / (1.0 + np.abs(want))
+    bound = tol * (1.0 + np.abs(want)) + rel * np.abs(want)
+    err = tol * np.abs(g - want) / bound
     worst = float(err.max()) if err.size else 0.0
     if worst > tol:
         idx = np.unravel_index(np.argmax(err), err.shape)
-        raise AssertionError(f"{what}: max rel err {worst:.3e} at {idx}: gpu {g[idx]!r} ref {want[idx]!r}")
+        raise AssertionError(f"{what}: error {worst / tol:.3f} x the bound at {idx}: gpu {g[idx]!r} ref {want[idx]!r}")
     return worst
 
 
@@ -49,9 +60,18 @@ def sample_rows(E, T, seed, limit=1 << 20, n=96):
 def _np(t, rows=None):
     if t is None:
         return None
+    if t.dtype == torch.bfloat16:  # exact in float32
+        t = t.float()
     if rows is None or t.dim() == 0:
         return t.cpu().numpy()
     return t[torch.as_tensor(rows, device=t.device)].cpu().numpy()
+
+
+def to_bf16(d):
+    """The float32 tensors of an input dict rounded to bfloat16 (the values
+    both sides then take as exact inputs)."""
+    return {k: (v.to(torch.bfloat16) if isinstance(v, torch.Tensor) and v.dtype == torch.float32 else v)
+            for k, v in d.items()}
 
 
 def _tm(d, time_major):
@@ -186,10 +206,14 @@ def run_oracle(kind, d, rows, params=None):
 
 
 def check_case(kind, E, T, seed=0, trunc=True, time_major=False, multipass=False, params=None, device="cuda",
-               gen_device=None, rows=None, inputs=None, inputs_ready=False, shift=False, **gen_kw):
-    """Run one parity case; returns the worst relative error seen."""
+               gen_device=None, rows=None, inputs=None, inputs_ready=False, shift=False, bf16=False, **gen_kw):
+    """Run one parity case; returns the worst relative error seen.  bf16:
+    inputs rounded to bfloat16 and passed as such (RLCA_BF16); outputs
+    checked against the oracle on those inputs with the rounding bound."""
     d = inputs if inputs is not None else make_inputs(kind, E, T, seed, trunc, gen_device or device, **gen_kw)
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    if bf16:
+        d = to_bf16(d)
     got = run_gpu(kind, d, time_major=time_major, multipass=multipass, params=params, inputs_ready=inputs_ready,
                   shift=shift)
     torch.cuda.synchronize()
@@ -200,6 +224,9 @@ def check_case(kind, E, T, seed=0, trunc=True, time_major=False, multipass=False
     for i, (g, w) in enumerate(zip(got, want)):
         if g is None:
             continue
+        if bf16 and g.dtype != torch.bfloat16 and g.is_floating_point():
+            raise AssertionError(f"{kind} out{i}: dtype {g.dtype}, expected bfloat16")
         worst = max(worst, assert_close(_np(g, rows), w, f"{kind} out{i} E={E} T={T} tm={time_major} "
-                                                          f"trunc={trunc} mp={multipass}"))
+                                                          f"trunc={trunc} mp={multipass} bf16={bf16}",
+                                        tol=BF16_TOL if bf16 else TOL, rel=BF16_REL if bf16 else 0.0))
     return worst

@@ -105,3 +105,22 @@ def test_invalid_arguments_other_entry_points(lib):
     assert lib.rlca_workspace_size(99, 4, 8, 0, 0, C.byref(out)) == INV
     assert lib.rlca_workspace_size(1, 4, 8, 0, 0, None) == INV
     assert lib.rlca_workspace_size(1, 0, 8, 0, 0, C.byref(out)) == _lib.RLCA_OK and out.value == 0
+
+
+def test_bf16_flag_scope(lib):
+    """RLCA_BF16 covers the float-storage calls; Retrace and the no-allocation
+    GAE keep float32 (unsupported), int32 prefix sums have no bfloat16 form,
+    and the overlap checks count 2-byte elements."""
+    INV, UNS, BF = _lib.RLCA_ERR_INVALID_ARG, _lib.RLCA_ERR_UNSUPPORTED, _lib.RLCA_BF16
+    P = [C.c_void_p(0x100000 * (i + 1)) for i in range(12)]
+    assert lib.rlca_retrace(P[0], P[1], P[2], P[3], P[4], None, None, None, None, P[5], 4, 8, 18,
+                            0.99, 0.95, BF, None, 0, None) == UNS
+    assert lib.rlca_gae_static_scratch(P[0], P[1], None, None, None, None, P[2], P[3], 4, 8, 0.99, 0.95, BF,
+                                       None) == UNS
+    assert lib.rlca_episodic_prefix_sum(P[0], _lib.RLCA_I32, None, None, P[1], 4, 8, BF, None, 0, None) == INV
+    # 4 x 8 bfloat16 elements span 64 bytes: an output 62 bytes in overlaps the input
+    assert lib.rlca_elig_trace(P[0], None, None, C.c_void_p(0x100000 + 62), 4, 8, 0.99, 0.9, BF, None, 0,
+                               None) == INV
+    out = C.c_size_t(1)
+    assert lib.rlca_workspace_size(1, 4, 8, 0, BF, C.byref(out)) in (_lib.RLCA_OK, _lib.RLCA_ERR_CUDA)
+

@@ -310,3 +310,52 @@ def test_workspace_sizes_consistent():
     d = parity.make_inputs("gae", 3, 40000, seed=1, trunc=False, device="cuda")
     with pytest.raises(ValueError):
         rlca.rlca_gae(d["rewards"], d["values"], workspace=torch.empty(8, dtype=torch.uint8, device="cuda"))
+
+
+# --------------------------------------------------------------------------
+# bfloat16 storage (RLCA_BF16): float32 arithmetic, outputs rounded once
+# --------------------------------------------------------------------------
+
+BF16_KINDS = ["gae", "vt", "disc", "td", "vtrace", "elig", "psum_f32", "affine_bwd", "affine_fwd"]
+
+
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
+@pytest.mark.parametrize("E,T", [(8, 16), (37, 129), (256, 128), (70, 1024), (5, 2048), (3, 40001)])
+@pytest.mark.parametrize("kind", BF16_KINDS)
+def test_bf16_storage(kind, E, T, tm):
+    """bfloat16 inputs and outputs through every driver: the fast drivers
+    (whole 4- or 8-step chunks), ragged T (scalar loads), one-tile and
+    multi-tile rows and the two-pass segments; against the oracle on the
+    same bfloat16 inputs within the rounding bound of parity.BF16_REL."""
+    parity.check_case(kind, E, T, seed=E * 131 + T, time_major=tm, bf16=True, p_term=0.02)
+
+
+@pytest.mark.parametrize("kind", BF16_KINDS)
+def test_bf16_wide_time_major_and_modes(kind):
+    """The staged time-major driver in bfloat16 (16-byte pieces of 8
+    environments: E % 8 == 0), its direct sibling (E % 8 != 0), the
+    inputs-ready and two-pass modes, and unaligned bfloat16 inputs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for E, seed in ((64 * sms + 8, 1), (64 * sms + 4, 2)):
+        parity.check_case(kind, E, 512, seed=seed, time_major=True, bf16=True, p_term=0.02)
+    parity.check_case(kind, 64 * sms + 8, 64, seed=3, time_major=True, bf16=True, inputs_ready=True)
+    parity.check_case(kind, 300, 256, seed=4, bf16=True, inputs_ready=True)
+    parity.check_case(kind, 6, 3000, seed=5, bf16=True, multipass=True)
+    parity.check_case(kind, 6, 3000, seed=6, bf16=True, multipass=True, time_major=True)
+    parity.check_case(kind, 36, 96, seed=7, bf16=True, shift=True)
+    parity.check_case(kind, 36, 96, seed=8, bf16=True, shift=True, time_major=True)
+
+
+def test_bf16_value_targets_4096x128():
+    """The fused value targets of the 4096 x 128 configuration in bfloat16."""
+    parity.check_case("vt", 4096, 128, seed=11, bf16=True)
+    parity.check_case("vt", 4096, 128, seed=12, bf16=True, inputs_ready=True)
+
+
+def test_bf16_retrace_is_unsupported():
+    d = parity.make_inputs("retrace", 4, 8, seed=1, trunc=True, device="cuda")
+    b = parity.to_bf16(d)
+    with pytest.raises(_lib.RlcaError):
+        rlca.rlca_retrace(b["q"], b["pi"], b["mu_a"], b["actions"], b["rewards"], b["terminated"],
+                          b["truncated"], b["trunc_value"], b["bootstrap"])
+
