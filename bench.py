@@ -483,32 +483,38 @@ SWEEP_SHAPES += [(E, T, tm, tr) for E in (256, 1024, 4096, 16384) for T in (32, 
                  for tm in (False, True) for tr in (False, True)]
 
 
-def _sweep_case(kind, E, T, trunc, dev):
+def _sweep_case(kind, E, T, trunc, dev, bf16=False):
     """Seeded inputs (env-major), the algorithmic bytes of one call, and the
-    output buffers' shapes and dtypes."""
+    output buffers' shapes and dtypes.  bf16: the float arrays are bfloat16
+    (RLCA_BF16), 2 bytes per element."""
     import torch
     from first_order_linear_gb300 import synth
     seed = synth.config_seed(f"bench-{kind}-{E}-{T}-{trunc}")
     A = synth.NUM_ACTIONS
-    f32 = torch.float32
+    fdt = torch.bfloat16 if bf16 else torch.float32
+    fe = 2 if bf16 else 4
     if kind in ("gae", "disc", "td", "vt"):
         d = synth.value_rollout(E, T, seed, p_term=P_TERM, p_trunc=P_TRUNC, with_trunc=trunc, device=dev)
-        reads = {"gae": 9, "disc": 5, "td": 9, "vt": 9}[kind]
+        reads = {"gae": 2, "disc": 1, "td": 2, "vt": 2}[kind] * fe + 1
         outs = {"gae": 2, "disc": 1, "td": 1, "vt": 4}[kind]
-        spec = [((E, T), f32)] * outs
+        spec = [((E, T), fdt)] * outs
     elif kind == "vtrace":
         d = synth.vtrace_rollout(E, T, seed, p_term=0.01, p_trunc=P_TRUNC if trunc else 0.0, with_trunc=trunc,
                                  device=dev)
-        reads, spec = 17, [((E, T), f32)] * 2
+        reads, spec = 4 * fe + 1, [((E, T), fdt)] * 2
     elif kind == "retrace":
         d = synth.retrace_rollout(E, T, seed, p_term=0.002, p_trunc=P_TRUNC if trunc else 0.0, with_trunc=trunc,
                                   device=dev)
-        reads, spec = 8 * A + 13, [((E, T), f32)]
+        reads, spec = 2 * A * fe + fe + 4 + fe + 1, [((E, T), fdt)]
     else:
         d = synth.forward_rollout(E, T, seed, p_term=0.01, p_trunc=P_TRUNC, with_trunc=trunc, device=dev)
-        reads, spec = 5, [((E, T), f32 if kind == "elig" else torch.int32)]
+        reads, spec = fe + 1, [((E, T), fdt if kind == "elig" else torch.int32)]
+    if bf16:
+        d = {k: (v.to(torch.bfloat16) if isinstance(v, torch.Tensor) and v.dtype == torch.float32 else v)
+             for k, v in d.items()}
     n_trunc = int(d["truncated"].sum()) if d.get("truncated") is not None else 0
-    per_step = reads + (1 if d.get("truncated") is not None else 0) + 4 * len(spec)
+    per_step = reads + (1 if d.get("truncated") is not None else 0) + sum(
+        torch.empty(0, dtype=dt).element_size() for _, dt in spec)
     tv_bytes = 32 * n_trunc if kind in ("gae", "disc", "td", "vt", "vtrace", "retrace") else 0
     return d, per_step * E * T + tv_bytes, spec
 
@@ -552,13 +558,15 @@ def run_sweep(args):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     peak, peak_kind = _peaks()
     kinds = args.sweep_kinds.split(",") if args.sweep_kinds else SWEEP_KINDS
+    if args.sweep_dtype == "bf16":  # Retrace and int32 prefix sums keep their storage
+        kinds = [k for k in kinds if k not in ("retrace", "psum")]
     shapes = SWEEP_SHAPES
     stream = torch.cuda.Stream(dev)
     for kind in kinds:
         for E, T, tm, trunc in shapes:
-            d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
+            d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev, bf16=args.sweep_dtype == "bf16")
             foot = sum(v.numel() * v.element_size() for v in d.values() if isinstance(v, torch.Tensor))
-            foot += sum(E * T * 4 for _ in spec)
+            foot += sum(E * T * torch.empty(0, dtype=dt).element_size() for _, dt in spec)
             nb = max(2, min(64, math.ceil(3 * l2 / foot)))
             src = {k: (synth.to_time_major(v) if tm and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
             reps = []
@@ -588,7 +596,7 @@ def run_sweep(args):
             gbps = nbytes / (us / 1e6) / 1e9
             gbps_ready = nbytes / (us_ready / 1e6) / 1e9
             print(json.dumps({"kind": kind, "E": E, "T": T, "layout": "time-major" if tm else "env-major",
-                              "trunc": trunc, "us_per_call": round(us, 3), "algorithmic_bytes": nbytes,
+                              "trunc": trunc, "dtype": args.sweep_dtype, "us_per_call": round(us, 3), "algorithmic_bytes": nbytes,
                               "GBps": round(gbps, 1), "frac_of_peak": round(gbps / peak, 4),
                               "us_per_call_inputs_ready": round(us_ready, 3),
                               "frac_of_peak_inputs_ready": round(gbps_ready / peak, 4),
@@ -631,6 +639,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="print one line per estimator and benchmark shape instead of the step metric")
     ap.add_argument("--sweep-kinds", default="", help="comma-separated subset of " + ",".join(SWEEP_KINDS))
+    ap.add_argument("--sweep-dtype", choices=["f32", "bf16"], default="f32",
+                    help="storage of the float arrays in --sweep (bf16: RLCA_BF16, float32 arithmetic)")
     ap.add_argument("--ncu-case", default="",
                     help="KIND,E,T,em|tm: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()

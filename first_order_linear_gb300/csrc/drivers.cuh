@@ -410,8 +410,24 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 // serial walk), and the chunk boundary values come back through shared
 // memory.  The scan lanes of an environment keep its carry across tiles.
 // ---------------------------------------------------------------------------
+// the 64-register cap of the fast time-major drivers pays where a kernel
+// needs only a few more; the staged V-Trace needs ~80 and runs faster
+// uncapped than spilling (its direct sibling is faster capped)
+template <class Est>
+struct TfRegCap {
+  static constexpr bool value = true;
+};
+template <bool H, class ST>
+struct TfRegCap<VtraceEst<H, ST>> {
+  static constexpr bool value = false;
+};
+template <class Est, int BLOCK>
+__host__ __device__ constexpr int tf_blocks_for() {
+  return TfRegCap<Est>::value ? tf_min_blocks(BLOCK) : 1;
+}
+
 template <class Est, int EW, int CT>
-__global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK)
+__global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<EW, CT>::BLOCK))
     tm_fast_kernel(Est est, Geom g) {
   using S = TfShape<EW, CT>;
   using V = typename Est::V;
@@ -519,7 +535,7 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK)
 // the fast time-major one; outputs go straight to global memory.
 // ---------------------------------------------------------------------------
 template <class Est, int EW, int CT>
-__global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK)
+__global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, TsShape<EW, CT>::BLOCK>()))
     tm_staged_kernel(Est est, Geom g) {
   using S = TsShape<EW, CT>;
   using V = typename Est::V;

@@ -48,9 +48,9 @@ struct Stor<float> {
   static constexpr int kBytes = 4;
   __device__ __forceinline__ static float ld(const float* p, int64_t i) { return __ldg(p + i); }
   __device__ __forceinline__ static void st(float* p, int64_t i, float v) { p[i] = v; }
-  // four consecutive elements starting at a 16-byte boundary
-  __device__ __forceinline__ static void ld4(const float* p, int64_t i, float* o) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
+  // four consecutive elements starting at a 16-byte boundary (zeros where !ok)
+  __device__ __forceinline__ static void ld4(const float* p, int64_t i, bool ok, float* o) {
+    const float4 v = ok ? __ldg(reinterpret_cast<const float4*>(p + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
     o[0] = v.x, o[1] = v.y, o[2] = v.z, o[3] = v.w;
   }
   __device__ __forceinline__ static void st4(float* p, int64_t i, const float* v) {
@@ -71,9 +71,10 @@ struct Stor<bf16> {
   __device__ __forceinline__ static void st(float* p, int64_t i, float v) {
     reinterpret_cast<unsigned short*>(p)[i] = (unsigned short)to_bits(v);
   }
-  // four consecutive elements starting at an 8-byte boundary
-  __device__ __forceinline__ static void ld4(const float* p, int64_t i, float* o) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(p) + i));
+  // four consecutive elements starting at an 8-byte boundary (zeros where !ok)
+  __device__ __forceinline__ static void ld4(const float* p, int64_t i, bool ok, float* o) {
+    const uint2 w =
+        ok ? __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(p) + i)) : make_uint2(0, 0);
     o[0] = __uint_as_float(w.x << 16), o[1] = __uint_as_float(w.x & 0xffff0000u);
     o[2] = __uint_as_float(w.y << 16), o[3] = __uint_as_float(w.y & 0xffff0000u);
   }
@@ -170,13 +171,7 @@ __device__ __forceinline__ void load_vals(const float* __restrict__ p, const Lay
   if (vec) {
     const int64_t base = lay.at(row, t0);
 #pragma unroll
-    for (int i = 0; i < L / 4; ++i) {
-      if (4 * i < n) {
-        Stor<ST>::ld4(p, base + 4 * i, &out[4 * i]);
-      } else {
-        out[4 * i] = out[4 * i + 1] = out[4 * i + 2] = out[4 * i + 3] = 0.f;
-      }
-    }
+    for (int i = 0; i < L / 4; ++i) Stor<ST>::ld4(p, base + 4 * i, 4 * i < n, &out[4 * i]);
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k) out[k] = (k < n) ? Stor<ST>::ld(p, lay.at(row, t0 + k)) : 0.f;
@@ -394,6 +389,12 @@ struct TfShape {
   static constexpr int PAD = EW + 1;  // row stride of the [CT][EW] exchange arrays
   static_assert(BLOCK % 32 == 0 && CT <= 32 && (CT & (CT - 1)) == 0, "chunk groups tile the warps");
 };
+// resident CTAs the fast time-major drivers are compiled for: 32 warps per
+// SM for CTAs of 128 threads or more, i.e. at most 64 registers a thread (a
+// few more cost a whole CTA); tiny CTAs (T < 32) are left unbounded
+__host__ __device__ constexpr int tf_min_blocks(int block) {
+  return block >= 1024 ? 1 : (1024 / block < 8 ? 1024 / block : 8);
+}
 template <class V, int EW, int CT>
 __host__ __device__ constexpr size_t tf_smem_bytes() {
   return (size_t)CT * TfShape<EW, CT>::PAD * (sizeof(Aff<V>) + sizeof(V));
