@@ -56,9 +56,12 @@ def _workload_config(extra=None):
     return cfg
 
 
-def _batch_cpu():
+def _batch_cpu(rank=0):
+    """This rank's shard of the job: environments [rank * E, (rank + 1) * E)
+    of a world * E environment batch, each shard from its own seed."""
     from first_order_linear_gb300 import synth
-    return synth.value_rollout(E, T, seed=synth.config_seed("4096x128"), p_term=P_TERM, p_trunc=P_TRUNC,
+    name = "4096x128" if rank == 0 else f"4096x128-shard{rank}"
+    return synth.value_rollout(E, T, seed=synth.config_seed(name), p_term=P_TERM, p_trunc=P_TRUNC,
                                with_trunc=True, device="cpu")
 
 
@@ -67,6 +70,24 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def _max_over_ranks(x, device):
+    """The largest x of all ranks (the job's time is its slowest rank's);
+    x itself when no process group is up."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(world, ms, steps):
+    """Whole-job throughput: every rank processed its own E x T shard per
+    step for every estimator, in the slowest rank's time."""
+    return world * N_EST * E * T * steps / (ms / 1e3)
 
 
 # --------------------------------------------------------------------------
@@ -296,7 +317,7 @@ def run_ours(args):
     from first_order_linear_gb300 import _lib, build
     build.build()
     lib = _lib.load()
-    d_cpu = _batch_cpu()
+    d_cpu = _batch_cpu(rank)
     d = {k: (v.to(dev) if v is not None else None) for k, v in d_cpu.items()}
 
     props = torch.cuda.get_device_properties(dev)
@@ -357,12 +378,9 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = _max_over_ranks(ms, dev)
     ms_per_step = ms / args.steps
-    value = world * N_EST * E * T * args.steps / (ms / 1e3)
+    value = _job_value(world, ms, args.steps)
 
     # per-kernel figures, each from a graph of one rotation of that launch
     kern = {}
