@@ -16,7 +16,7 @@ enum class Kind { Gae, Disc, TdLambda, Vtrace, Retrace, Elig, PrefixSum, Affine,
 // per-action blocks in shared memory).
 constexpr int kEmMaxWidth = 1024;
 constexpr int kTmMaxWidth = 32;
-constexpr int kRetraceEmMaxWidth = 128;
+constexpr int kRetraceEmMaxWidth = 256;
 constexpr int kRetraceTmMaxWidth = 8;
 constexpr int kEmMinWidth = 1;
 constexpr size_t kMaxSmemPerCta = 227 * 1024;
