@@ -214,10 +214,12 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   }
   // time-major rows of whole 8-step chunks with 32-bit element offsets take
   // the fast time-major driver in one pass: 32 environments per CTA once that
-  // still leaves two CTAs per SM, else 8 (32-byte row pieces, 4x the CTAs).
-  // Few environments with many tiles each keep the segmented split instead.
+  // still leaves two CTAs per SM, else one 32-byte sector of a step row (8
+  // float32 or 16 bfloat16 environments; more CTAs).  Few environments with
+  // many tiles each keep the segmented split instead.
   const int ct_need = next_pow2((T + 7) / 8);
-  const int tf_ew = (E >= (int64_t)64 * sm_count || ct_need < 4) ? 32 : 8;
+  // narrow CTAs read one 32-byte sector of a step row: 8 float32 or 16 bfloat16 environments
+  const int tf_ew = (E >= (int64_t)64 * sm_count || ct_need < 4) ? 32 : (bf16_io ? 16 : 8);
   const int tf_ct = std::min(ct_need, tf_ew == 32 ? 16 : 32);
   const int64_t tf_threads = (E + tf_ew - 1) / tf_ew * tf_ew * tf_ct;
   const bool tf_few = q.nseg > 1 && tf_threads < (int64_t)sm_count * 128 && T > 4 * 8 * tf_ct;

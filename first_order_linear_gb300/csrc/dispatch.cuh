@@ -126,6 +126,19 @@ static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, c
       default: return cudaErrorInvalidConfiguration;
     }
   }
+  if constexpr (sizeof(typename Est::Store) == 2) {
+    // 2-byte storage: 16 environments make a 32-byte sector of a step row
+    if (p.env_width == 16) {
+      switch (p.width) {
+        case 2: return launch_tf<Est, 16, 2>(p, est, g, s);
+        case 4: return launch_tf<Est, 16, 4>(p, est, g, s);
+        case 8: return launch_tf<Est, 16, 8>(p, est, g, s);
+        case 16: return launch_tf<Est, 16, 16>(p, est, g, s);
+        case 32: return launch_tf<Est, 16, 32>(p, est, g, s);
+        default: return cudaErrorInvalidConfiguration;
+      }
+    }
+  }
   if (p.env_width == 8) {
     switch (p.width) {
       case 4: return launch_tf<Est, 8, 4>(p, est, g, s);
