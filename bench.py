@@ -668,12 +668,14 @@ def run_ncu_case(args):
     capture with ``-s 2 -c 1``)."""
     import torch
     from first_order_linear_gb300 import build, synth
-    kind, E, T, lay = args.ncu_case.split(",")
+    parts = args.ncu_case.split(",")
+    kind, E, T, lay = parts[:4]
+    bf16 = len(parts) > 4 and parts[4] == "bf16"
     E, T, tm = int(E), int(T), lay == "tm"
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    d, nbytes, spec = _sweep_case(kind, E, T, True, dev)
+    d, nbytes, spec = _sweep_case(kind, E, T, True, dev, bf16=bf16)
     x = {k: (synth.to_time_major(v) if tm and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     o = [torch.empty(sh if not tm else (sh[1], sh[0]), dtype=dt, device=dev) for sh, dt in spec]
     for _ in range(4):
@@ -697,7 +699,7 @@ def main():
     ap.add_argument("--sweep-dtype", choices=["f32", "bf16"], default="f32",
                     help="storage of the float arrays in --sweep (bf16: RLCA_BF16, float32 arithmetic)")
     ap.add_argument("--ncu-case", default="",
-                    help="KIND,E,T,em|tm: four calls of one estimator on one batch (a case for ncu), no timing")
+                    help="KIND,E,T,em|tm[,bf16]: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

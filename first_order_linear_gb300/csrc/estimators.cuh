@@ -498,14 +498,24 @@ struct RetraceStage {
     float mu;
   };
   // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous): the
-  // warp's Q and pi blocks go to shared memory as asynchronous 4-byte copies,
-  // all in flight at once and committed as one group; the taken action and
-  // mu(a_t) load into registers alongside
+  // warp's Q and pi blocks go to shared memory as asynchronous copies, all in
+  // flight at once and committed as one group -- 16-byte pieces when both
+  // blocks start on a 16-byte boundary (the shared buffers always do), else
+  // 4-byte ones; the taken action and mu(a_t) load into registers alongside
   __device__ __forceinline__ Pending issue(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p) const {
     const float* qb = q + e0 * A;
     const float* pb = pi + e0 * A;
     const int total = cnt * A;
-    for (int f = lane; f < total; f += 32) {
+    int f0 = 0;
+    if (((reinterpret_cast<uintptr_t>(qb) | reinterpret_cast<uintptr_t>(pb)) & 15u) == 0) {
+      const int n4 = total >> 2;
+      for (int f = lane; f < n4; f += 32) {
+        cp_async16(raw_q + 4 * f, qb + 4 * f);
+        cp_async16(raw_p + 4 * f, pb + 4 * f);
+      }
+      f0 = 4 * n4;
+    }
+    for (int f = f0 + lane; f < total; f += 32) {
       cp_async4(raw_q + f, qb + f);
       cp_async4(raw_p + f, pb + f);
     }
@@ -524,7 +534,17 @@ struct RetraceStage {
       const float* rq = raw_q + lane * A;
       const float* rp = raw_p + lane * A;
       float ev = 0.f;
-      for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
+      if ((A & 1) == 0) {  // 8-byte aligned pairs, same summation order
+        const float2* q2 = reinterpret_cast<const float2*>(rq);
+        const float2* p2 = reinterpret_cast<const float2*>(rp);
+        for (int a = 0; a < A / 2; ++a) {
+          const float2 x = q2[a], y = p2[a];
+          ev = fmaf(y.x, x.x, ev);
+          ev = fmaf(y.y, x.y, ev);
+        }
+      } else {
+        for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
+      }
       const int at = pd.at < 0 ? 0 : (pd.at >= A ? A - 1 : pd.at);
       dst_ev[slot] = ev;
       dst_qa[slot] = rq[at];
