@@ -176,10 +176,11 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     nseg = q.ntiles >= 2 ? (q.ntiles + 1) / 2 : 1;
   } else {
     // split long rows across CTAs only when the rows alone leave the GPU
-    // mostly idle; the second pass re-reads the inputs
+    // mostly idle; the second pass re-reads the inputs (for Retrace, 161
+    // bytes a step: it splits only when the rows are 8x fewer still)
     const int64_t threads = q.row_blocks * q.block;
     const int64_t target = (int64_t)sm_count * 1024;
-    if (q.ntiles > 1 && 2 * threads < target)
+    if (q.ntiles > 1 && 2 * threads < target && (!retrace || 16 * threads < target))
       nseg = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
   }
   const int seg_tiles = (q.ntiles + nseg - 1) / nseg;
