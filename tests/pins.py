@@ -106,6 +106,36 @@ def _combine(outer, inner):
     return (aB + bB * aA, bA * bB)
 
 
+def pin_combine_algebra(ref):
+    """The combine of §2.2 is associative ((X+Y)+Z = X+(Y+Z) on random
+    tuples), has the identity (0, 1), and a reset (alpha, 0) absorbs what it
+    is composed with (§5: beta = 0 severs the carry); and the oracle's
+    recurrence over a row equals the combine of its recurrences over the two
+    parts of any split of the row (the regrouping every parallel scan relies
+    on).  A segment's map is (A with carry 0, change of A per unit carry)."""
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        X, Y, Z = (tuple(rng.normal(size=2)) for _ in range(3))
+        _close(np.array(_combine(_combine(X, Y), Z)), np.array(_combine(X, _combine(Y, Z))), tol=1e-12,
+               what="associativity")
+        _close(np.array(_combine(X, (0.0, 1.0))), np.array(X), tol=1e-15, what="right identity")
+        _close(np.array(_combine((0.0, 1.0), X)), np.array(X), tol=1e-15, what="left identity")
+        _close(np.array(_combine((X[0], 0.0), Y)), np.array((X[0], 0.0)), tol=1e-15, what="reset absorbs")
+    for T in (2, 5, 9):
+        a = rng.normal(size=(1, T))
+        b = rng.uniform(-1.2, 1.2, size=(1, T))
+
+        def seg_map(lo, hi):
+            zero = ref.affine_scan(a[:, lo:hi], b[:, lo:hi], np.zeros(1), reverse=True)[0, 0]
+            one = ref.affine_scan(a[:, lo:hi], b[:, lo:hi], np.ones(1), reverse=True)[0, 0]
+            return (zero, one - zero)
+
+        whole = seg_map(0, T)
+        for k in range(1, T):
+            _close(np.array(_combine(seg_map(0, k), seg_map(k, T))), np.array(whole), tol=1e-10,
+                   what=f"split T={T} at {k}")
+
+
 def load_app_a_trace():
     rows = []
     with open(os.path.join(GOLDEN, "app_a_four_thread_trace.txt")) as f:
