@@ -301,6 +301,69 @@ def test_empty_inputs():
     assert rlca.rlca_discounted_return(z2).shape == (5, 0)
 
 
+# --------------------------------------------------------------------------
+# large sizes: 64-bit offsets and very long rows (against the C reference,
+# which walks long rows quickly; a few sampled rows of the wide cases)
+# --------------------------------------------------------------------------
+
+def _big_flags(shape, p, gen):
+    return (torch.rand(shape, device="cuda", dtype=torch.float16, generator=gen) < p).to(torch.uint8)
+
+
+def _check_rows(got, want, what):
+    parity.assert_close(got, want, what)
+
+
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
+def test_element_offsets_beyond_32_bits(tm):
+    """E * T past 2^31 (env-major) and past 2^32 (time-major: the 32-bit
+    offset drivers step aside for the general ones): discounted returns and
+    eligibility traces on sampled environments.  About 40 GB on the device."""
+    from oracle import ref_c
+    gen = torch.Generator(device="cuda").manual_seed(99)
+    E, T = (65539, 32771) if not tm else (131075, 32771)
+    shape = (T, E) if tm else (E, T)
+    r = torch.randn(shape, device="cuda", generator=gen)
+    term = _big_flags(shape, 0.001, gen)
+    rows = np.array([0, 1, E // 2, E - 1])
+    pick = (lambda t: t[:, torch.as_tensor(rows, device="cuda")].T) if tm else \
+        (lambda t: t[torch.as_tensor(rows, device="cuda")])
+    r_s, term_s = pick(r).double().cpu().numpy(), pick(term).cpu().numpy()
+    out = rlca.rlca_discounted_return(r, term, time_major=tm)
+    torch.cuda.synchronize()
+    _check_rows(pick(out).double().cpu().numpy(), ref_c.discounted_return(r_s, term_s, gamma=parity.GAMMA),
+                f"disc E={E} T={T} tm={tm}")
+    del out
+    out = rlca.rlca_elig_trace(r, term, time_major=tm)
+    torch.cuda.synchronize()
+    _check_rows(pick(out).double().cpu().numpy(),
+                ref_c.eligibility_trace(r_s, term_s, gamma=parity.GAMMA, lam=parity.LAMBDA),
+                f"elig E={E} T={T} tm={tm}")
+    del out, r, term
+    torch.cuda.empty_cache()
+
+
+def test_rows_of_a_hundred_million_steps():
+    """T = 2^27 + 5 on two environments: the segmented two-pass path (each
+    segment hundreds of tiles long, unaligned row ends), backward and
+    forward."""
+    from oracle import ref_c
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    E, T = 2, (1 << 27) + 5
+    r = torch.randn(E, T, device="cuda", generator=gen)
+    term = _big_flags((E, T), 1e-6, gen)
+    r_h, term_h = r.double().cpu().numpy(), term.cpu().numpy()
+    out = rlca.rlca_discounted_return(r, term)
+    torch.cuda.synchronize()
+    _check_rows(out.double().cpu().numpy(), ref_c.discounted_return(r_h, term_h, gamma=parity.GAMMA), "disc")
+    out = rlca.rlca_elig_trace(r, term)
+    torch.cuda.synchronize()
+    _check_rows(out.double().cpu().numpy(),
+                ref_c.eligibility_trace(r_h, term_h, gamma=parity.GAMMA, lam=parity.LAMBDA), "elig")
+    del out, r, term
+    torch.cuda.empty_cache()
+
+
 def test_workspace_sizes_consistent():
     assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 4096, 128) == 0
     assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, 3, 40000) > 0
