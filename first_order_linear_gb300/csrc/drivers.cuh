@@ -160,45 +160,23 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
 }
 
 // ---------------------------------------------------------------------------
-// fast env-major driver: the common case compiled without run-time
-// generality.  Preconditions (checked by the planner): 16-byte aligned rows,
-// T % LS == 0 and T <= TILE (one tile per row), one segment, one pass.
-// A thread therefore holds either all LS steps or none, and a thread
-// beyond its row's end contributes the identity map to the scan.
+// the fast env-major driver's scan of one row group whose inputs are in R:
+// neighbour exchange, coefficients, warp scan, cross-warp exchange through
+// xw ([ROWS][NWR] slots, one CTA barrier), re-expansion into R's outputs.
+// Every thread of the CTA calls it (the barrier).
 // ---------------------------------------------------------------------------
 template <class Est, int TPR, int LS>
-__global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
-    em_fast_kernel(Est est, Geom g) {
+__device__ __forceinline__ void em_fast_scan(const Est& est, typename Est::template Regs<EmShape<TPR, LS>::L>& R,
+                                             const Geom& g, const EnvMajor& lay, int64_t row, int t0, bool active,
+                                             int rloc, Aff<typename Est::V>* xw) {
   using S = EmShape<TPR, LS>;
   using V = typename Est::V;
   constexpr bool BWD = Est::kBackward;
   constexpr int L = S::L, GW = S::GW, NWR = S::NWR;
-
-  extern __shared__ __align__(16) unsigned char smem[];
-  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);  // [ROWS][NWR] warp totals (NWR > 1)
-  unsigned char* est_smem = smem + (NWR > 1 ? 2 * S::ROWS * NWR * sizeof(Aff<V>) : 0);
-
-  const int tid = threadIdx.x;
-  const int j = tid % TPR;
-  const int rloc = tid / TPR;
-  const int lane = tid & 31;
+  const int j = threadIdx.x % TPR;
+  const int lane = threadIdx.x & 31;
   const int lig = j % GW;
   const int wr = j / 32;
-  const int64_t row0 = (int64_t)blockIdx.x * S::ROWS;
-  const int64_t row = row0 + rloc;
-  const int t0 = j * L;
-  const bool active = row < g.E && t0 < g.T;
-  const int n = active ? L : 0;
-  const EnvMajor lay{g.E, g.T};
-  const bool early = g.early != 0;
-  if (!early) pdl_wait();
-
-  est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, 0, g.T, est_smem);
-  typename Est::template Regs<L> R;
-  const GIO<EnvMajor, true, typename Est::Store> io{lay, row, t0, n, true};
-  est.template load<L>(R, io, rloc, 0, S::TILE, S::ROWS, est_smem);
-  pdl_trigger();
-
   if constexpr (Est::kNb > 0) {
     float give[Est::kNb > 0 ? Est::kNb : 1], got[Est::kNb > 0 ? Est::kNb : 1];
     est.nb_give(R, give);
@@ -283,6 +261,45 @@ __global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
       est.emit(R, k, A, adj, c[k]);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// fast env-major driver: the common case compiled without run-time
+// generality.  Preconditions (checked by the planner): 16-byte aligned rows,
+// T % LS == 0 and T <= TILE (one tile per row), one segment, one pass.
+// A thread therefore holds either all LS steps or none, and a thread
+// beyond its row's end contributes the identity map to the scan.
+// ---------------------------------------------------------------------------
+template <class Est, int TPR, int LS>
+__global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
+    em_fast_kernel(Est est, Geom g) {
+  using S = EmShape<TPR, LS>;
+  using V = typename Est::V;
+  constexpr int L = S::L, NWR = S::NWR;
+
+  extern __shared__ __align__(16) unsigned char smem[];
+  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);  // [ROWS][NWR] warp totals (NWR > 1)
+  unsigned char* est_smem = smem + (NWR > 1 ? 2 * S::ROWS * NWR * sizeof(Aff<V>) : 0);
+
+  const int tid = threadIdx.x;
+  const int j = tid % TPR;
+  const int rloc = tid / TPR;
+  const int64_t row0 = (int64_t)blockIdx.x * S::ROWS;
+  const int64_t row = row0 + rloc;
+  const int t0 = j * L;
+  const bool active = row < g.E && t0 < g.T;
+  const int n = active ? L : 0;
+  const EnvMajor lay{g.E, g.T};
+  const bool early = g.early != 0;
+  if (!early) pdl_wait();
+
+  est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, 0, g.T, est_smem);
+  typename Est::template Regs<L> R;
+  const GIO<EnvMajor, true, typename Est::Store> io{lay, row, t0, n, true};
+  est.template load<L>(R, io, rloc, 0, S::TILE, S::ROWS, est_smem);
+  pdl_trigger();
+
+  em_fast_scan<Est, TPR, LS>(est, R, g, lay, row, t0, active, rloc, xw);
   if (early) pdl_wait();  // the previous kernel may still read or write what we overwrite
   if (active) est.template store<L>(R, io);
 }

@@ -124,6 +124,17 @@ def test_time_major_chunk_groups(kind, T):
 
 
 @pytest.mark.parametrize("kind", parity.KINDS)
+@pytest.mark.parametrize("T", [16, 64, 256, 1024])
+def test_more_row_groups_than_one_wave(kind, T):
+    """Single-tile env-major calls with many waves of CTAs (hundreds of
+    thousands of rows, ragged E), in both stream modes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    E = 40 * sms * 4096 // max(T, 64) + 5
+    parity.check_case(kind, E, T, seed=T + 31, p_term=0.02)
+    parity.check_case(kind, E, T, seed=T + 32, p_term=0.02, inputs_ready=True)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
 @pytest.mark.parametrize("T", [1024, 3072, 4096])
 def test_long_single_tile_rows(kind, T):
     """Rows of 1024-4096 steps fit one tile.  With few environments the fast
