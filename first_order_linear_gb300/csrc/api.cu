@@ -196,8 +196,13 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   // Retrace's per-warp staging keeps fewer CTAs resident, so it switches only
   // once four times as many threads are in flight
   const int64_t l8_min_threads = (int64_t)sm_count * 1024 * (retrace ? 4 : 1);
-  if (fast_ok && T >= kFastL8MinT && T % 8 == 0 && (int64_t)E * (T / 8) >= l8_min_threads &&
-      W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
+  // bfloat16 rows take 8 steps a thread from 64 steps on (one 16-byte vector
+  // per array, the bytes a float32 thread moves with 4) once the threads
+  // still fill the GPU; V-Trace, whose four inputs cost occupancy, keeps the
+  // float32 rule
+  const int l8_min_t = (bf16_io && kind != Kind::Vtrace) ? 64 : kFastL8MinT;
+  const bool l8 = T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads;
+  if (fast_ok && l8 && T % 8 == 0 && W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
     // long rows on enough environments: 8 steps per thread halves the warps per row
     q.fast = true;
     q.steps = 8;

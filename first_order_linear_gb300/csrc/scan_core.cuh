@@ -82,6 +82,20 @@ struct Stor<bf16> {
     const uint2 w = make_uint2(to_bits(v[0]) | (to_bits(v[1]) << 16), to_bits(v[2]) | (to_bits(v[3]) << 16));
     *reinterpret_cast<uint2*>(reinterpret_cast<unsigned short*>(p) + i) = w;
   }
+  // eight consecutive elements starting at a 16-byte boundary (zeros where !ok)
+  __device__ __forceinline__ static void ld8(const float* p, int64_t i, bool ok, float* o) {
+    const uint4 w =
+        ok ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p) + i)) : make_uint4(0, 0, 0, 0);
+    o[0] = __uint_as_float(w.x << 16), o[1] = __uint_as_float(w.x & 0xffff0000u);
+    o[2] = __uint_as_float(w.y << 16), o[3] = __uint_as_float(w.y & 0xffff0000u);
+    o[4] = __uint_as_float(w.z << 16), o[5] = __uint_as_float(w.z & 0xffff0000u);
+    o[6] = __uint_as_float(w.w << 16), o[7] = __uint_as_float(w.w & 0xffff0000u);
+  }
+  __device__ __forceinline__ static void st8(float* p, int64_t i, const float* v) {
+    const uint4 w = make_uint4(to_bits(v[0]) | (to_bits(v[1]) << 16), to_bits(v[2]) | (to_bits(v[3]) << 16),
+                               to_bits(v[4]) | (to_bits(v[5]) << 16), to_bits(v[6]) | (to_bits(v[7]) << 16));
+    *reinterpret_cast<uint4*>(reinterpret_cast<unsigned short*>(p) + i) = w;
+  }
 };
 
 // x -> a + b * x
@@ -170,8 +184,13 @@ __device__ __forceinline__ void load_vals(const float* __restrict__ p, const Lay
                                           int t0, int n, bool vec, float (&out)[L]) {
   if (vec) {
     const int64_t base = lay.at(row, t0);
+    if constexpr (sizeof(ST) == 2 && L % 8 == 0) {  // 16-byte vectors of 8 bfloat16 steps
 #pragma unroll
-    for (int i = 0; i < L / 4; ++i) Stor<ST>::ld4(p, base + 4 * i, 4 * i < n, &out[4 * i]);
+      for (int i = 0; i < L / 8; ++i) Stor<ST>::ld8(p, base + 8 * i, 8 * i < n, &out[8 * i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < L / 4; ++i) Stor<ST>::ld4(p, base + 4 * i, 4 * i < n, &out[4 * i]);
+    }
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k) out[k] = (k < n) ? Stor<ST>::ld(p, lay.at(row, t0 + k)) : 0.f;
@@ -232,9 +251,15 @@ __device__ __forceinline__ void store_vals(float* __restrict__ p, const Lay& lay
                                            int n, bool vec, const float (&v)[L]) {
   if (vec) {
     const int64_t base = lay.at(row, t0);
+    if constexpr (sizeof(ST) == 2 && L % 8 == 0) {
 #pragma unroll
-    for (int i = 0; i < L / 4; ++i)
-      if (4 * i < n) Stor<ST>::st4(p, base + 4 * i, &v[4 * i]);
+      for (int i = 0; i < L / 8; ++i)
+        if (8 * i < n) Stor<ST>::st8(p, base + 8 * i, &v[8 * i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < L / 4; ++i)
+        if (4 * i < n) Stor<ST>::st4(p, base + 4 * i, &v[4 * i]);
+    }
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k)
