@@ -200,8 +200,10 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   // per array, the bytes a float32 thread moves with 4) once the threads
   // still fill the GPU; V-Trace, whose four inputs cost occupancy, keeps the
   // float32 rule
+  // float32 rows of 256-1023 steps take them too with twice the threads
   const int l8_min_t = (bf16_io && kind != Kind::Vtrace) ? 64 : kFastL8MinT;
-  const bool l8 = T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads;
+  const bool l8 = (T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads) ||
+                  (!bf16_io && kind != Kind::Vtrace && T >= 256 && (int64_t)E * (T / 8) >= 2 * l8_min_threads);
   if (fast_ok && l8 && T % 8 == 0 && W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
     // long rows on enough environments: 8 steps per thread halves the warps per row
     q.fast = true;

@@ -76,7 +76,7 @@ static cudaError_t launch_fast_wl(const Plan& p, const Est& est, const Geom& g, 
 template <class Est, int W>
 static cudaError_t launch_fast_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if (p.steps == 8) {
-    if constexpr (W >= 64 || (sizeof(typename Est::Store) == 2 && W >= 8)) return launch_fast_wl<Est, W, 8>(p, est, g, s);
+    if constexpr (W >= 32 || (sizeof(typename Est::Store) == 2 && W >= 8)) return launch_fast_wl<Est, W, 8>(p, est, g, s);
     return cudaErrorInvalidConfiguration;
   }
   return launch_fast_wl<Est, W, kEmSteps>(p, est, g, s);

@@ -135,6 +135,17 @@ def test_more_row_groups_than_one_wave(kind, T):
 
 
 @pytest.mark.parametrize("kind", parity.KINDS)
+@pytest.mark.parametrize("T", [256, 512])
+def test_mid_rows_eight_steps_a_thread(kind, T):
+    """Rows of 256-1023 steps on environments that fill the GPU twice over
+    take 8 steps a thread (one or two warps a row), ragged E."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    E = -(-2 * sms * 1024 // (T // 8)) + 3
+    parity.check_case(kind, E, T, seed=T + 41, p_term=0.02)
+    parity.check_case(kind, E, T, seed=T + 42, p_term=0.02, inputs_ready=True)
+
+
+@pytest.mark.parametrize("kind", parity.KINDS)
 @pytest.mark.parametrize("T", [1024, 3072, 4096])
 def test_long_single_tile_rows(kind, T):
     """Rows of 1024-4096 steps fit one tile.  With few environments the fast
