@@ -238,8 +238,15 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     // of 64-step tiles.  With 8
     // environments per CTA the rows are single 32-byte sectors and reading
     // them straight into registers is faster.
-    const bool staged = kTmStaged && vec && E % (bf16_io ? 8 : 4) == 0 && tf_ew == 32;
-    const int EW = tf_ew, CT = staged ? std::min(tf_ct, tf_ew == 32 ? 8 : 32) : tf_ct;
+    const bool staged32 = kTmStaged && vec && E % (bf16_io ? 8 : 4) == 0 && tf_ew == 32;
+    // float32 narrow CTAs of the one-float-input scans: staged in 64-byte
+    // rows of 16 environments (measured faster there; with two or more
+    // float inputs the direct 8-environment driver wins)
+    const bool one_float = kind == Kind::Disc || kind == Kind::Elig || kind == Kind::PrefixSum;
+    const bool staged16 = kTmStaged16 && one_float && vec && !bf16_io && E % 4 == 0 && tf_ew == 8;
+    const bool staged = staged32 || staged16;
+    const int EW = staged16 ? 16 : tf_ew;
+    const int CT = staged32 ? std::min(tf_ct, 8) : tf_ct;
     q.tm_fast = true;
     q.tm_staged = staged;
     q.env_width = EW;

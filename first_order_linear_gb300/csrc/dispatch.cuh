@@ -111,7 +111,18 @@ static cudaError_t launch_ts_any(const Plan& p, const Est& est, const Geom& g, c
       default: return cudaErrorInvalidConfiguration;
     }
   }
-  return cudaErrorInvalidConfiguration;  // the planner stages 32-environment tiles only
+  if constexpr (sizeof(typename Est::Store) == 4) {
+    if (p.env_width == 16) {
+      switch (p.width) {
+        case 4: return launch_ts<Est, 16, 4>(p, est, g, s);
+        case 8: return launch_ts<Est, 16, 8>(p, est, g, s);
+        case 16: return launch_ts<Est, 16, 16>(p, est, g, s);
+        case 32: return launch_ts<Est, 16, 32>(p, est, g, s);
+        default: return cudaErrorInvalidConfiguration;
+      }
+    }
+  }
+  return cudaErrorInvalidConfiguration;
 }
 
 template <class Est>

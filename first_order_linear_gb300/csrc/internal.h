@@ -53,6 +53,12 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
 // build-time choice: aligned time-major inputs stream through shared memory
 // (tm_staged_kernel) rather than straight into registers (tm_fast_kernel)
 constexpr bool kTmStaged = RLCA_TM_STAGED != 0;
+#ifndef RLCA_TM_STAGED16
+#define RLCA_TM_STAGED16 1
+#endif
+// ... also for float32 tiles of 16 environments (rows of 64 bytes) where the
+// direct driver would take 8
+constexpr bool kTmStaged16 = RLCA_TM_STAGED16 != 0;
 
 #ifndef RLCA_STAGED_PATH
 #define RLCA_STAGED_PATH 0
