@@ -425,6 +425,13 @@ def run_ours(args):
                           "launches (one launch per step; consecutive launches overlap)"}
 
     e2e = None if args.skip_e2e else run_e2e(args, d_cpu, dev)
+    if e2e is not None and world > 1:
+        # whole job: every rank's shard through its own host link, in the
+        # slowest rank's time
+        e2e_ms = _max_over_ranks(e2e["ms_per_step"], dev)
+        e2e.update(ms_per_step=e2e_ms, value=world * N_EST * E * T / (e2e_ms / 1e3),
+                   h2d_bytes_per_step=world * e2e["h2d_bytes_per_step"],
+                   d2h_bytes_per_step=world * e2e["d2h_bytes_per_step"], ranks=world)
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         cpu = cpu_baseline(d_cpu)
