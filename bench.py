@@ -350,8 +350,7 @@ def run_ours(args):
     rem_n = args.steps % nb
     rem = _capture(reps[:rem_n], [fused], stream) if rem_n else None
 
-    sampler = ClockSampler(dev.index, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(dev.index, args.clock_log or None)
     sampler.start()
     with torch.cuda.stream(stream):
         for _ in range(max(1, math.ceil(args.warmup / nb))):
@@ -695,7 +694,7 @@ def run_ncu_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
@@ -703,6 +702,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="print one line per estimator and benchmark shape instead of the step metric")
     ap.add_argument("--sweep-kinds", default="", help="comma-separated subset of " + ",".join(SWEEP_KINDS))
+    ap.add_argument("--clock-log", default="", help="also write the nvidia-smi clock samples of the timed region "
+                                                    "to this CSV file")
     ap.add_argument("--sweep-dtype", choices=["f32", "bf16"], default="f32",
                     help="storage of the float arrays in --sweep (bf16: RLCA_BF16, float32 arithmetic)")
     ap.add_argument("--ncu-case", default="",
