@@ -192,20 +192,19 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const bool fast_ok = !q.staged && !q.time_major && vec && q.nseg == 1 && !(flags & RLCA_MULTIPASS);
   q.fast = fast_ok && T % kEmSteps == 0 && q.ntiles == 1;
   q.steps = kEmSteps;
+  // 8 steps a thread (half the warps and scan rounds a row) where the
+  // threads still fill the GPU: rows of >= 1024 steps (Retrace, whose
+  // per-warp staging keeps fewer CTAs resident, at four times the threads);
+  // float32 rows of 256-1023 steps at twice the threads; bfloat16 rows from
+  // 64 steps on (one 16-byte vector per array, the bytes a float32 thread
+  // moves with 4).  V-Trace, whose four inputs cost occupancy, takes only
+  // the first rule.
   const int W8 = next_pow2((T + 7) / 8);
-  // Retrace's per-warp staging keeps fewer CTAs resident, so it switches only
-  // once four times as many threads are in flight
   const int64_t l8_min_threads = (int64_t)sm_count * 1024 * (retrace ? 4 : 1);
-  // bfloat16 rows take 8 steps a thread from 64 steps on (one 16-byte vector
-  // per array, the bytes a float32 thread moves with 4) once the threads
-  // still fill the GPU; V-Trace, whose four inputs cost occupancy, keeps the
-  // float32 rule
-  // float32 rows of 256-1023 steps take them too with twice the threads
   const int l8_min_t = (bf16_io && kind != Kind::Vtrace) ? 64 : kFastL8MinT;
   const bool l8 = (T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads) ||
                   (!bf16_io && kind != Kind::Vtrace && T >= 256 && (int64_t)E * (T / 8) >= 2 * l8_min_threads);
   if (fast_ok && l8 && T % 8 == 0 && W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
-    // long rows on enough environments: 8 steps per thread halves the warps per row
     q.fast = true;
     q.steps = 8;
     q.ntiles = 1;
@@ -233,15 +232,12 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const bool tf_few = q.nseg > 1 && tf_threads < (int64_t)sm_count * 128 && T > 4 * 8 * tf_ct;
   if (q.time_major && !retrace && !tf_few && T % 8 == 0 && !(flags & RLCA_MULTIPASS) &&
       (uint64_t)E * (uint64_t)T < (uint64_t{1} << 32)) {
-    // staged: 16-byte pieces of the step rows of 32 environments (E a
-    // multiple of the environments per piece, aligned inputs) through a ring
-    // of 64-step tiles.  With 8
-    // environments per CTA the rows are single 32-byte sectors and reading
-    // them straight into registers is faster.
+    // staged: the step rows stream through a shared-memory ring in 16-byte
+    // pieces (E a multiple of the environments per piece, aligned inputs):
+    // rows of 32 environments in 64-step tiles; for the one-float-input
+    // scans also rows of 16.  Otherwise the rows go straight into registers.
     const bool staged32 = kTmStaged && vec && E % (bf16_io ? 8 : 4) == 0 && tf_ew == 32;
-    // float32 narrow CTAs of the one-float-input scans: staged in 64-byte
-    // rows of 16 environments (measured faster there; with two or more
-    // float inputs the direct 8-environment driver wins)
+    // (with two or more float inputs the direct 8-environment driver measured faster)
     const bool one_float = kind == Kind::Disc || kind == Kind::Elig || kind == Kind::PrefixSum;
     const bool staged16 = kTmStaged16 && one_float && vec && !bf16_io && E % 4 == 0 && tf_ew == 8;
     const bool staged = staged32 || staged16;
