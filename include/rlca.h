@@ -32,9 +32,10 @@
  *    every [E, T] array is [T, E] (e fastest) and every per-action array is
  *    [T, E, A] instead of [E, T, A].  Per-environment vectors (bootstrap,
  *    carry) are [E] in both layouts.  Arrays are dense and contiguous.
- *  - Element types: float32 values, uint8 flags (nonzero = set), int32
- *    actions.  Any pointer alignment is accepted; 16-byte aligned rows
- *    (T % 4 == 0, aligned bases) take the vectorised load path.
+ *  - Element types: float32 values (bfloat16 with RLCA_BF16), uint8 flags
+ *    (nonzero = set), int32 actions.  Any pointer alignment is accepted;
+ *    16-byte aligned bases with T % 4 == 0 take the vectorised load paths
+ *    (env-major rows; time-major rows staged through shared memory).
  *  - Sizes: 0 <= E <= 2^31-1, 0 <= T <= 2^30.
  *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *    call returns without synchronising.  No host or device memory is
@@ -54,8 +55,8 @@
  *  - Errors: RLCA_ERR_INVALID_ARG (NULL required pointer, negative or
  *    oversized E/T, overlapping outputs, workspace too small or misaligned,
  *    unknown flags) and RLCA_ERR_UNSUPPORTED (num_actions above
- *    RLCA_MAX_ACTIONS) are detected on the host before anything is
- *    enqueued.  RLCA_ERR_CUDA reports a failed CUDA runtime call (device
+ *    RLCA_MAX_ACTIONS, RLCA_BF16 where noted) are detected on the host
+ *    before anything is enqueued.  RLCA_ERR_CUDA reports a failed CUDA runtime call (device
  *    query or launch); the CUDA error itself is left readable through
  *    cudaGetLastError()/cudaPeekAtLastError().
  *  - Entry points are thread-safe and hold no global state except a
@@ -224,7 +225,9 @@ int rlca_value_targets(const float *rewards, const float *values,
  *    every slot the second pass reads.  Calls whose work overlaps on the GPU
  *    (other streams, other host threads) race on the array and give wrong
  *    results: serialise them.
- * Arguments, layouts, flags and errors otherwise as rlca_gae.
+ * Flags: RLCA_TIME_MAJOR and RLCA_MULTIPASS (RLCA_INPUTS_READY and other
+ * bits: RLCA_ERR_INVALID_ARG; RLCA_BF16: RLCA_ERR_UNSUPPORTED).  Arguments,
+ * layouts and errors otherwise as rlca_gae.
  */
 #define RLCA_STATIC_SCRATCH_BYTES (1u << 20)
 
