@@ -220,17 +220,15 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
                (size_t)3 * q.rows_per_cta * (q.tile + 1) * 4;
   }
   // time-major rows of whole 8-step chunks with 32-bit element offsets take
-  // the fast time-major driver in one pass: 32 environments per CTA once that
-  // still leaves two CTAs per SM, else one 32-byte sector of a step row (8
-  // float32 or 16 bfloat16 environments; more CTAs).  Few environments with
-  // many tiles each keep the segmented split instead.
+  // the fast time-major drivers: 32 environments per CTA once that still
+  // leaves two CTAs per SM, else one 32-byte sector of a step row (8 float32
+  // or 16 bfloat16 environments; more CTAs); few environments with long rows
+  // split them into segments (two passes).
   const int ct_need = next_pow2((T + 7) / 8);
   // narrow CTAs read one 32-byte sector of a step row: 8 float32 or 16 bfloat16 environments
   const int tf_ew = (E >= (int64_t)64 * sm_count || ct_need < 4) ? 32 : (bf16_io ? 16 : 8);
   const int tf_ct = std::min(ct_need, tf_ew == 32 ? 16 : 32);
-  const int64_t tf_threads = (E + tf_ew - 1) / tf_ew * tf_ew * tf_ct;
-  const bool tf_few = q.nseg > 1 && tf_threads < (int64_t)sm_count * 128 && T > 4 * 8 * tf_ct;
-  if (q.time_major && !retrace && !tf_few && T % 8 == 0 && !(flags & RLCA_MULTIPASS) &&
+  if (q.time_major && !retrace && T % 8 == 0 && !(flags & RLCA_MULTIPASS) &&
       (uint64_t)E * (uint64_t)T < (uint64_t{1} << 32)) {
     // staged: the step rows stream through a shared-memory ring in 16-byte
     // pieces (E a multiple of the environments per piece, aligned inputs):
@@ -251,14 +249,22 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.rows_per_cta = EW;
     q.tile = 8 * CT;
     q.ntiles = (T + q.tile - 1) / q.tile;
-    q.nseg = 1;
-    q.seg_len = q.ntiles * q.tile;
     q.row_blocks = (E + EW - 1) / EW;
+    // the two-pass split when the environments alone leave the GPU mostly
+    // idle and each would walk more than four tiles (a shorter walk costs
+    // less than the second read of the inputs)
+    const int64_t threads = q.row_blocks * q.block;
+    const int64_t target = (int64_t)sm_count * 1024;
+    int ns = 1;
+    if (q.ntiles > 4 && 2 * threads < target) ns = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
+    const int seg_tiles = (q.ntiles + ns - 1) / ns;
+    q.seg_len = seg_tiles * q.tile;
+    q.nseg = (q.ntiles + seg_tiles - 1) / seg_tiles;
+    q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
     q.smem = 0;
     q.smem_driver_bound = (size_t)CT * (EW + 1) * (kMaxMapBytes + kMaxMapBytes / 2);
     // the stages: at most 4 float and 2 flag inputs of CT * (8 * EW + EW) elements
     if (staged) q.smem_driver_bound += (size_t)RLCA_TS_STAGES * ((size_t)CT * 9 * EW * 18 + 16);
-    q.ws_bytes = 0;
   }
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;

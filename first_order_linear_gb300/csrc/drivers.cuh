@@ -420,7 +420,9 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 
 // ---------------------------------------------------------------------------
 // fast time-major driver.  Preconditions (checked by the planner): T % L == 0,
-// E * T < 2^32, one segment, one pass.  Each tile of CT * L steps: every
+// E * T < 2^32; few environments with long rows run it as the two-pass
+// segmented split (segment maps, then the segments from their entering
+// values), like the general drivers.  Each tile of CT * L steps: every
 // thread composes its chunk's L maps from coalesced step rows (EW
 // consecutive environments per load), the CT chunk maps of an environment are
 // scanned by CT adjacent lanes with shuffles (log2 CT rounds instead of a
@@ -458,21 +460,32 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
   const int tid = threadIdx.x;
   const int j = tid % EW, c = tid / EW;    // load / emit role
   const int js = tid / CT, cs = tid % CT;  // scan role
-  const int64_t row0 = (int64_t)blockIdx.x * EW;
+  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
+  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * EW;
   const int64_t row = row0 + j;
   const bool row_ok = row < g.E;
+  const int seg_lo = seg * g.seg_len;
+  const int seg_hi = min(g.T, seg_lo + g.seg_len);
+  const bool agg_mode = g.mode == kModeAggregate;
   const uint32_t E32 = (uint32_t)g.E;
   const TimeMajor lay{g.E, g.T};
-  const bool early = g.early != 0;
+  const bool early = g.early != 0 && g.nseg == 1;
   if (!early) pdl_wait();
 
-  V carry = row0 + js < g.E ? est.row_carry(row0 + js) : V(0);
-  const int ntiles = (g.T + S::TILE - 1) / S::TILE;
+  // scan role: the value entering this segment (full pass) or the map of
+  // the whole segment (first pass of the two-pass path)
+  V carry = V(0);
+  Aff<V> seg_map = aff_identity<V>();
+  if (!agg_mode && row0 + js < g.E) {
+    carry = est.row_carry(row0 + js);
+    if (g.nseg > 1) carry = segment_carry_in<V, BWD>(g, row0 + js, seg, carry);
+  }
+  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
   for (int it = 0; it < ntiles; ++it) {
     const int tile = BWD ? ntiles - 1 - it : it;
-    const int ts = tile * S::TILE;
+    const int ts = seg_lo + tile * S::TILE;
     const int t0 = ts + c * L;
-    const int n = (row_ok && t0 < g.T) ? L : 0;
+    const int n = (row_ok && t0 < seg_hi) ? L : 0;
     const TmIO32<typename Est::Store> io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32};
 
     typename Est::template Regs<L> R;
@@ -517,9 +530,14 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
     Aff<V> ex = BWD ? shfl_down_aff(m, 1, CT) : shfl_up_aff(m, 1, CT);
     if (cs == (BWD ? CT - 1 : 0)) ex = aff_identity<V>();
     const Aff<V> tot = shfl_idx_aff(m, BWD ? 0 : CT - 1, CT);
-    ys[cs * PAD + js] = ex.a + ex.b * carry;
-    carry = tot.a + tot.b * carry;
+    if (agg_mode) {
+      seg_map = compose(tot, seg_map);  // tiles arrive in the order the recurrence applies them
+    } else {
+      ys[cs * PAD + js] = ex.a + ex.b * carry;
+      carry = tot.a + tot.b * carry;
+    }
     __syncthreads();
+    if (agg_mode) continue;
 
     V A = ys[c * PAD + j];
     if (BWD) {
@@ -540,11 +558,14 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
     if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
     est.template store<L>(R, io);
   }
+  if (agg_mode && cs == 0 && row0 + js < g.E)
+    reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
 
 // ---------------------------------------------------------------------------
 // staged time-major driver.  Preconditions: those of the fast time-major
-// driver, E % 4 == 0, 16-byte aligned float inputs and 4-byte aligned flag
+// driver (the two-pass split included), E a multiple of the environments of
+// a 16-byte piece, 16-byte aligned float inputs and 4-byte aligned flag
 // inputs.  The inputs of the tiles stream into a ring of NS shared-memory
 // stages with cp.async (16-byte pieces of a step row for floats, 4-byte
 // pieces for flags), NS - 1 tiles ahead of the tile being scanned, so the
@@ -577,24 +598,28 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
   const int tid = threadIdx.x;
   const int j = tid % EW, c = tid / EW;    // load / emit role
   const int js = tid / CT, cs = tid % CT;  // scan role
-  const int64_t row0 = (int64_t)blockIdx.x * EW;
+  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
+  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * EW;
   const int64_t row = row0 + j;
   const bool row_ok = row < g.E;
+  const int seg_lo = seg * g.seg_len;
+  const int seg_hi = min(g.T, seg_lo + g.seg_len);
+  const bool agg_mode = g.mode == kModeAggregate;
   const uint32_t E32 = (uint32_t)g.E;
   const uint32_t e0 = (uint32_t)row0;
   const TimeMajor lay{g.E, g.T};
-  const bool early = g.early != 0;
+  const bool early = g.early != 0 && g.nseg == 1;
   if (!early) pdl_wait();
 
   StagedList in;
   est.staged_io(in);
-  const int ntiles = (g.T + S::TILE - 1) / S::TILE;
+  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
 
   // issue the copies of the it-th tile in processing order into stage it % NS
   // (one commit group per call, empty past the last tile)
   auto stage_tile = [&](int it) {
     if (it < ntiles) {
-      const int ts = (BWD ? ntiles - 1 - it : it) * S::TILE;
+      const int ts = seg_lo + (BWD ? ntiles - 1 - it : it) * S::TILE;
       unsigned char* st = ring + (size_t)(it % NS) * STAGE;
       // float inputs: 16-byte pieces of FPE environments (E % FPE == 0: a
       // piece is wholly inside or outside the rows)
@@ -637,9 +662,9 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
 #pragma unroll
     for (int i = 0; i < NB; ++i) got[i] = 0.f;
     if (Est::kNb > 0 && it < ntiles) {
-      const int t0 = (BWD ? ntiles - 1 - it : it) * S::TILE + c * L;
+      const int t0 = seg_lo + (BWD ? ntiles - 1 - it : it) * S::TILE + c * L;
       const int tn = BWD ? t0 + L : t0 - 1;
-      if (row_ok && t0 < g.T && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (row_ok && t0 < seg_hi && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
     }
   };
 
@@ -650,16 +675,23 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
   cp_async_wait<NS - 2>();
   __syncthreads();
 
-  V carry = row0 + js < g.E ? est.row_carry(row0 + js) : V(0);
+  // scan role: the value entering this segment (full pass) or the map of
+  // the whole segment (first pass of the two-pass path)
+  V carry = V(0);
+  Aff<V> seg_map = aff_identity<V>();
+  if (!agg_mode && row0 + js < g.E) {
+    carry = est.row_carry(row0 + js);
+    if (g.nseg > 1) carry = segment_carry_in<V, BWD>(g, row0 + js, seg, carry);
+  }
   for (int it = 0; it < ntiles; ++it) {
     stage_tile(it + NS - 1);  // into the stage every thread finished reading in iteration it - 1
     float nb_nxt[NB];
     nb_fetch(it + 1, nb_nxt);
     if (it == ntiles - 1) pdl_trigger();
     const int tile = BWD ? ntiles - 1 - it : it;
-    const int ts = tile * S::TILE;
+    const int ts = seg_lo + tile * S::TILE;
     const int t0 = ts + c * L;
-    const int n = (row_ok && t0 < g.T) ? L : 0;
+    const int n = (row_ok && t0 < seg_hi) ? L : 0;
     const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
     const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
                            (uint32_t)t0 * E32 + (uint32_t)row, E32};
@@ -698,10 +730,15 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     Aff<V> ex = BWD ? shfl_down_aff(m, 1, CT) : shfl_up_aff(m, 1, CT);
     if (cs == (BWD ? CT - 1 : 0)) ex = aff_identity<V>();
     const Aff<V> tot = shfl_idx_aff(m, BWD ? 0 : CT - 1, CT);
-    ys[cs * PAD + js] = ex.a + ex.b * carry;
-    carry = tot.a + tot.b * carry;
+    if (agg_mode) {
+      seg_map = compose(tot, seg_map);  // tiles arrive in the order the recurrence applies them
+    } else {
+      ys[cs * PAD + js] = ex.a + ex.b * carry;
+      carry = tot.a + tot.b * carry;
+    }
     cp_async_wait<NS - 2>();  // this thread's copies of tile it + 1 have landed
     __syncthreads();          // ... everyone's, and the chunk entry values are visible
+    if (agg_mode) continue;
 
     V A = ys[c * PAD + j];
     if (BWD) {
@@ -722,6 +759,8 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
     est.template store<L>(R, io);
   }
+  if (agg_mode && cs == 0 && row0 + js < g.E)
+    reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
 
 // ---------------------------------------------------------------------------

@@ -123,6 +123,17 @@ def test_time_major_chunk_groups(kind, T):
         parity.check_case(kind, E, T, seed=T * 11 + seed, time_major=True, p_term=0.02, inputs_ready=True)
 
 
+@pytest.mark.parametrize("kind", [k for k in parity.KINDS if k != "retrace"])
+@pytest.mark.parametrize("E,T", [(5, 40000), (12, 8192), (300, 4096), (1023, 2048)])
+def test_time_major_two_pass_fast_drivers(kind, E, T):
+    """Few environments with long whole-chunk rows, time-major: the fast and
+    staged time-major drivers run the two-pass split (segment maps, then the
+    segments from their entering values); direct (E % 4 != 0) and staged
+    tiles, both stream modes."""
+    parity.check_case(kind, E, T, seed=E + T, time_major=True, p_term=0.005)
+    parity.check_case(kind, E, T, seed=E + T + 1, time_major=True, p_term=0.005, inputs_ready=True)
+
+
 @pytest.mark.parametrize("kind", parity.KINDS)
 @pytest.mark.parametrize("T", [16, 64, 256, 1024])
 def test_more_row_groups_than_one_wave(kind, T):
