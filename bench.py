@@ -619,8 +619,8 @@ def run_sweep(args):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     peak, peak_kind = _peaks()
     kinds = args.sweep_kinds.split(",") if args.sweep_kinds else SWEEP_KINDS
-    if args.sweep_dtype == "bf16":  # Retrace and int32 prefix sums keep their storage
-        kinds = [k for k in kinds if k not in ("retrace", "psum")]
+    if args.sweep_dtype == "bf16":  # int32 prefix sums keep their storage
+        kinds = [k for k in kinds if k != "psum"]
     shapes = SWEEP_SHAPES
     stream = torch.cuda.Stream(dev)
     for kind in kinds:

@@ -498,27 +498,29 @@ int rlca_retrace(const float* q, const float* pi, const float* mu_a, const int32
   int st;
   if (check_sizes(E, T, &st)) return st;
   if (!flags_ok(flags, kFloatFlags)) return RLCA_ERR_INVALID_ARG;
-  if (flags & RLCA_BF16) return RLCA_ERR_UNSUPPORTED;
   if (num_actions < 1) return RLCA_ERR_INVALID_ARG;
   if (num_actions > RLCA_MAX_ACTIONS) return RLCA_ERR_UNSUPPORTED;
   if (!q || !pi || !mu_a || !actions || !rewards || !q_ret || (truncated && !trunc_value))
     return RLCA_ERR_INVALID_ARG;
-  const size_t nf = (size_t)(E * T) * 4, nb = (size_t)(E * T), nq = nf * (size_t)num_actions;
-  if (any_overlap({{q, nq}, {pi, nq}, {mu_a, nf}, {actions, nf}, {rewards, nf}, {terminated, nb}, {truncated, nb},
-                   {trunc_value, nf}, {bootstrap, (size_t)E * 4}, {workspace, workspace_bytes}},
+  const size_t fe = fbytes(flags), nf = (size_t)(E * T) * fe, nb = (size_t)(E * T), nq = nf * (size_t)num_actions;
+  if (any_overlap({{q, nq}, {pi, nq}, {mu_a, nf}, {actions, (size_t)(E * T) * 4}, {rewards, nf}, {terminated, nb},
+                   {truncated, nb}, {trunc_value, nf}, {bootstrap, (size_t)E * fe}, {workspace, workspace_bytes}},
                   {{q_ret, nf}}))
     return RLCA_ERR_INVALID_ARG;
   const bool vec = aligned(rewards, 16) && aligned(q_ret, 16) && aligned(terminated, 4) && aligned(truncated, 4);
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
-  const RetraceStage stg{q, pi, mu_a, actions, num_actions, lambda};
-  if (truncated) {
-    RetraceEst<true> e;
+  return with_storage(flags, [&](auto tag) {
+    using ST = typename decltype(tag)::type;
+    const RetraceStage<ST> stg{q, pi, mu_a, actions, num_actions, lambda};
+    if (truncated) {
+      RetraceEst<true, ST> e;
+      e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;
+      return launch(Kind::Retrace, e, E, T, num_actions, flags, workspace, workspace_bytes, vec, stream);
+    }
+    RetraceEst<false, ST> e;
     e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;
     return launch(Kind::Retrace, e, E, T, num_actions, flags, workspace, workspace_bytes, vec, stream);
-  }
-  RetraceEst<false> e;
-  e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;
-  return launch(Kind::Retrace, e, E, T, num_actions, flags, workspace, workspace_bytes, vec, stream);
+  });
 }
 
 int rlca_elig_trace(const float* x, const uint8_t* terminated, const uint8_t* truncated, float* out, int64_t E,

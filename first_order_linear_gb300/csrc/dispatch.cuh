@@ -11,8 +11,8 @@ struct WidthCaps {
   static constexpr int tm = kTmMaxWidth;
   static constexpr bool tm_fast = true;
 };
-template <bool H>
-struct WidthCaps<RetraceEst<H>> {
+template <bool H, class ST>
+struct WidthCaps<RetraceEst<H, ST>> {
   static constexpr int em = kRetraceEmMaxWidth;
   static constexpr int tm = kRetraceTmMaxWidth;
   static constexpr bool tm_fast = false;  // stages its per-action blocks per tile

@@ -485,10 +485,13 @@ __host__ __device__ constexpr int retrace_raw_floats(int A, bool time_major) {
   return retrace_bufs(time_major) * 64 * A;
 }
 
+template <class ST = float>
 struct RetraceStage {
-  const float* q;
-  const float* pi;
-  const float* mu_a;
+  static constexpr int ES = (int)sizeof(ST);  // bytes of a stored element
+  using Bits = typename std::conditional<ES == 2, unsigned short, uint32_t>::type;
+  const float* q;     // [.., A] elements of type ST
+  const float* pi;    // [.., A] elements of type ST
+  const float* mu_a;  // elements of type ST
   const int32_t* act;
   int A;
   float lambda;
@@ -497,33 +500,55 @@ struct RetraceStage {
     int at;
     float mu;
   };
-  // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous): the
-  // warp's Q and pi blocks go to shared memory as asynchronous copies, all in
-  // flight at once and committed as one group -- 16-byte pieces when both
-  // blocks start on a 16-byte boundary (the shared buffers always do), else
-  // 4-byte ones; the taken action and mu(a_t) load into registers alongside
-  __device__ __forceinline__ Pending issue(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p) const {
-    const float* qb = q + e0 * A;
-    const float* pb = pi + e0 * A;
-    const int total = cnt * A;
-    int f0 = 0;
-    if (((reinterpret_cast<uintptr_t>(qb) | reinterpret_cast<uintptr_t>(pb)) & 15u) == 0) {
-      const int n4 = total >> 2;
-      for (int f = lane; f < n4; f += 32) {
-        cp_async16(raw_q + 4 * f, qb + 4 * f);
-        cp_async16(raw_p + 4 * f, pb + 4 * f);
+  // bytes [b0, nbytes) of a block into shared memory: 16-byte asynchronous
+  // pieces while both sources allow them, then 4-byte pieces, then (an
+  // unaligned block, or the last half word of a bfloat16 one) plain loads
+  __device__ __forceinline__ static void copy_block(unsigned char* dq, unsigned char* dp, const unsigned char* qb,
+                                                    const unsigned char* pb, int nbytes, int lane) {
+    int b0 = 0;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(qb) | reinterpret_cast<uintptr_t>(pb);
+    if ((al & 15u) == 0) {
+      const int n16 = nbytes >> 4;
+      for (int f = lane; f < n16; f += 32) {
+        cp_async16(dq + 16 * f, qb + 16 * f);
+        cp_async16(dp + 16 * f, pb + 16 * f);
       }
-      f0 = 4 * n4;
+      b0 = 16 * n16;
     }
-    for (int f = f0 + lane; f < total; f += 32) {
-      cp_async4(raw_q + f, qb + f);
-      cp_async4(raw_p + f, pb + f);
+    if ((al & 3u) == 0) {
+      const int n4 = nbytes >> 2;
+      for (int f = (b0 >> 2) + lane; f < n4; f += 32) {
+        cp_async4(dq + 4 * f, qb + 4 * f);
+        cp_async4(dp + 4 * f, pb + 4 * f);
+      }
+      b0 = 4 * n4;
     }
+    for (int f = b0 / ES + lane; f < nbytes / ES; f += 32) {
+      reinterpret_cast<Bits*>(dq)[f] = __ldg(reinterpret_cast<const Bits*>(qb) + f);
+      reinterpret_cast<Bits*>(dp)[f] = __ldg(reinterpret_cast<const Bits*>(pb) + f);
+    }
+  }
+  // items e0 .. e0+cnt-1 (element indices of [.., A] rows, contiguous): the
+  // warp's Q and pi blocks go to shared memory, the copies all in flight at
+  // once and committed as one group (the shared buffers start on 16-byte
+  // boundaries); the taken action and mu(a_t) load into registers alongside
+  __device__ __forceinline__ Pending issue(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p) const {
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(q) + e0 * A * ES;
+    const unsigned char* pb = reinterpret_cast<const unsigned char*>(pi) + e0 * A * ES;
+    copy_block(reinterpret_cast<unsigned char*>(raw_q), reinterpret_cast<unsigned char*>(raw_p), qb, pb,
+               cnt * A * ES, lane);
     cp_async_commit();
     Pending pd;
     pd.at = lane < cnt ? __ldg(act + e0 + lane) : 0;
-    pd.mu = lane < cnt ? __ldg(mu_a + e0 + lane) : 1.f;
+    pd.mu = lane < cnt ? Stor<ST>::ld(mu_a, e0 + lane) : 1.f;
     return pd;
+  }
+  __device__ __forceinline__ static float elem(const float* raw, int i) {
+    if constexpr (ES == 4) {
+      return raw[i];
+    } else {
+      return __uint_as_float((uint32_t)reinterpret_cast<const Bits*>(raw)[i] << 16);
+    }
   }
   // once the chunk's copies have landed: item `lane` writes its three
   // scalars at index `slot` of the dst arrays
@@ -531,24 +556,37 @@ struct RetraceStage {
                                          const float* raw_p, float* dst_ev, float* dst_qa, float* dst_c,
                                          int slot) const {
     if (lane < cnt) {
-      const float* rq = raw_q + lane * A;
-      const float* rp = raw_p + lane * A;
+      const int base = lane * A;
       float ev = 0.f;
-      if ((A & 1) == 0) {  // 8-byte aligned pairs, same summation order
-        const float2* q2 = reinterpret_cast<const float2*>(rq);
-        const float2* p2 = reinterpret_cast<const float2*>(rp);
+      if constexpr (ES == 4) {
+        const float* rq = raw_q + base;
+        const float* rp = raw_p + base;
+        if ((A & 1) == 0) {  // 8-byte aligned pairs, same summation order
+          const float2* q2 = reinterpret_cast<const float2*>(rq);
+          const float2* p2 = reinterpret_cast<const float2*>(rp);
+          for (int a = 0; a < A / 2; ++a) {
+            const float2 x = q2[a], y = p2[a];
+            ev = fmaf(y.x, x.x, ev);
+            ev = fmaf(y.y, x.y, ev);
+          }
+        } else {
+          for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
+        }
+      } else if ((A & 1) == 0) {  // 4-byte aligned pairs of bfloat16, same summation order
+        const uint32_t* q2 = reinterpret_cast<const uint32_t*>(raw_q) + base / 2;
+        const uint32_t* p2 = reinterpret_cast<const uint32_t*>(raw_p) + base / 2;
         for (int a = 0; a < A / 2; ++a) {
-          const float2 x = q2[a], y = p2[a];
-          ev = fmaf(y.x, x.x, ev);
-          ev = fmaf(y.y, x.y, ev);
+          const uint32_t x = q2[a], y = p2[a];
+          ev = fmaf(__uint_as_float(y << 16), __uint_as_float(x << 16), ev);
+          ev = fmaf(__uint_as_float(y & 0xffff0000u), __uint_as_float(x & 0xffff0000u), ev);
         }
       } else {
-        for (int a = 0; a < A; ++a) ev = fmaf(rp[a], rq[a], ev);
+        for (int a = 0; a < A; ++a) ev = fmaf(elem(raw_p, base + a), elem(raw_q, base + a), ev);
       }
       const int at = pd.at < 0 ? 0 : (pd.at >= A ? A - 1 : pd.at);
       dst_ev[slot] = ev;
-      dst_qa[slot] = rq[at];
-      dst_c[slot] = lambda * fminf(1.f, rp[at] / pd.mu);
+      dst_qa[slot] = elem(raw_q, base + at);
+      dst_c[slot] = lambda * fminf(1.f, elem(raw_p, base + at) / pd.mu);
     }
   }
   // walks chunks warp, warp + NW, ... < nch; where(ch, &e0, &cnt, &slot)
@@ -601,16 +639,16 @@ struct RetraceStage {
   }
 };
 
-template <bool HAS_TRUNC>
+template <bool HAS_TRUNC, class ST = float>
 struct RetraceEst {
-  using Store = float;
+  using Store = ST;
   using V = float;
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
   static constexpr bool kStageable = false;
   static constexpr int kSF = 0, kSB = 0, kSO = 0;  // staged float inputs, flag inputs, outputs
   BoundaryArgs b;
-  RetraceStage st;
+  RetraceStage<ST> st;
   const float* r;
   float* out;
   float gamma;
@@ -676,7 +714,7 @@ struct RetraceEst {
   __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int slot, int ts, int tile, int nrows,
                                        unsigned char* sm) const {
     io.template f<L>(0, r, R.r);
-    load_boundary<HAS_TRUNC, float, L>(b, R.bd, io);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
     constexpr bool kTM = IO::kTimeMajor;
     const int t0 = io.t0, n = io.n;
     const int NW = blockDim.x >> 5;

@@ -11,7 +11,7 @@ sets RLCA_INPUTS_READY (the inputs were not written by the kernel just before
 this call on the stream, so the call may overlap it).  Flags may be uint8 or
 bool tensors; ``None`` means "no such flag" for the optional inputs.  Float
 tensors are float32, or all bfloat16 (RLCA_BF16: bfloat16 storage, float32
-arithmetic, outputs rounded once; not for Retrace).
+arithmetic, outputs rounded once).
 """
 from __future__ import annotations
 

@@ -103,8 +103,9 @@ typedef struct CUstream_st *rlca_stream_t;
  * Arithmetic and the scan state stay float32; each output is rounded to
  * nearest-even bfloat16 once.  Flags and int32 arrays are unchanged.  With
  * rlca_episodic_prefix_sum it applies to RLCA_F32 data only (RLCA_I32:
- * RLCA_ERR_INVALID_ARG); rlca_retrace and rlca_gae_static_scratch return
- * RLCA_ERR_UNSUPPORTED.  The paper defers bfloat16 I/O to future work and
+ * RLCA_ERR_INVALID_ARG); rlca_gae_static_scratch returns
+ * RLCA_ERR_UNSUPPORTED.  With rlca_retrace it covers q, pi and mu_a as well
+ * (the expectation and the ratio are formed in float32).  The paper defers bfloat16 I/O to future work and
  * keeps scans in float32 (rl-triton (arXiv:2608.17641) §9 Discussion and
  * Future Work; §4 Implementation, numerical requirements): only storage is
  * narrowed here. */

@@ -108,13 +108,14 @@ def test_invalid_arguments_other_entry_points(lib):
 
 
 def test_bf16_flag_scope(lib):
-    """RLCA_BF16 covers the float-storage calls; Retrace and the no-allocation
-    GAE keep float32 (unsupported), int32 prefix sums have no bfloat16 form,
-    and the overlap checks count 2-byte elements."""
+    """RLCA_BF16 covers the float-storage calls; the no-allocation GAE keeps
+    float32 (unsupported), int32 prefix sums have no bfloat16 form, and the
+    overlap checks count 2-byte elements."""
     INV, UNS, BF = _lib.RLCA_ERR_INVALID_ARG, _lib.RLCA_ERR_UNSUPPORTED, _lib.RLCA_BF16
     P = [C.c_void_p(0x100000 * (i + 1)) for i in range(12)]
-    assert lib.rlca_retrace(P[0], P[1], P[2], P[3], P[4], None, None, None, None, P[5], 4, 8, 18,
-                            0.99, 0.95, BF, None, 0, None) == UNS
+    # 4 x 8 x 18 bfloat16 Q values span 1152 bytes: an output 1150 bytes in overlaps them
+    assert lib.rlca_retrace(P[0], P[1], P[2], P[3], P[4], None, None, None, None, C.c_void_p(0x100000 + 1150),
+                            4, 8, 18, 0.99, 0.95, BF, None, 0, None) == INV
     assert lib.rlca_gae_static_scratch(P[0], P[1], None, None, None, None, P[2], P[3], 4, 8, 0.99, 0.95, BF,
                                        None) == UNS
     assert lib.rlca_episodic_prefix_sum(P[0], _lib.RLCA_I32, None, None, P[1], 4, 8, BF, None, 0, None) == INV

@@ -412,7 +412,7 @@ def test_workspace_sizes_consistent():
 # bfloat16 storage (RLCA_BF16): float32 arithmetic, outputs rounded once
 # --------------------------------------------------------------------------
 
-BF16_KINDS = ["gae", "vt", "disc", "td", "vtrace", "elig", "psum_f32", "affine_bwd", "affine_fwd"]
+BF16_KINDS = ["gae", "vt", "disc", "td", "vtrace", "retrace", "elig", "psum_f32", "affine_bwd", "affine_fwd"]
 
 
 @pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
@@ -448,10 +448,12 @@ def test_bf16_value_targets_4096x128():
     parity.check_case("vt", 4096, 128, seed=12, bf16=True, inputs_ready=True)
 
 
-def test_bf16_retrace_is_unsupported():
-    d = parity.make_inputs("retrace", 4, 8, seed=1, trunc=True, device="cuda")
-    b = parity.to_bf16(d)
-    with pytest.raises(_lib.RlcaError):
-        rlca.rlca_retrace(b["q"], b["pi"], b["mu_a"], b["actions"], b["rewards"], b["terminated"],
-                          b["truncated"], b["trunc_value"], b["bootstrap"])
+@pytest.mark.parametrize("A", [1, 3, 18, 64])
+@pytest.mark.parametrize("tm", [False, True], ids=["env", "time"])
+def test_bf16_retrace_action_counts(A, tm):
+    """bfloat16 Q and pi blocks of every parity of A: odd A leaves the
+    per-step blocks 2-byte aligned (4-byte and plain-load copies), A = 64
+    the 16-byte pieces."""
+    parity.check_case("retrace", 40, 200, seed=A, time_major=tm, bf16=True, num_actions=A)
+    parity.check_case("retrace", 40, 200, seed=A + 1, time_major=tm, bf16=True, num_actions=A, shift=True)
 
