@@ -668,6 +668,178 @@ def run_sweep(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# The vectorised PyTorch doubling-scan baseline: the form of comparison the
+# paper quotes its speed-ups against (rl-triton (arXiv:2608.17641) §1
+# Introduction, §7 Results): each estimator's (alpha, beta) built with
+# whole-tensor torch ops, then log2(T) recursive-doubling passes of affine
+# map composition over the whole [E, T] tensor.  Env-major, float32 (int32
+# for the prefix sum).  A measurement baseline only: the library never runs
+# it.
+# ---------------------------------------------------------------------------
+
+def torch_doubling_scan(alpha, beta, reverse=True):
+    """A_t = alpha_t + beta_t * A_{t+1} (reverse) or A_{t-1} (forward) along
+    the last dim, carry 0.  After the pass of stride s, (A_t, B_t) is the
+    composition of the 2s maps from step t on (reverse) or back to it; maps
+    past the row's end count as the identity."""
+    import torch
+    A, B = alpha, beta
+    T = A.shape[-1]
+    s = 1
+    while s < T:
+        if reverse:
+            A = torch.cat([A[..., :-s] + B[..., :-s] * A[..., s:], A[..., -s:]], -1)
+            B = torch.cat([B[..., :-s] * B[..., s:], B[..., -s:]], -1)
+        else:
+            A = torch.cat([A[..., :s], A[..., s:] + B[..., s:] * A[..., :-s]], -1)
+            B = torch.cat([B[..., :s], B[..., s:] * B[..., :-s]], -1)
+        s *= 2
+    return A
+
+
+def _torch_edges(x, term, trunc):
+    """Per-step masks of the boundary rules: truncated (and not terminated),
+    continues into t+1 inside the window, ends the window unflagged."""
+    import torch
+    T = x.shape[-1]
+    tm = term.bool() if term is not None else torch.zeros_like(x, dtype=torch.bool)
+    tr = (trunc.bool() & ~tm) if trunc is not None else torch.zeros_like(tm)
+    inner = torch.arange(T, device=x.device) < T - 1
+    free = ~tm & ~tr
+    return tr, free & inner, free & ~inner
+
+
+def _torch_next(x, last):
+    import torch
+    return torch.cat([x[..., 1:], last[..., None]], -1)
+
+
+def torch_doubling(kind, x, gamma=GAMMA, lam=LAMBDA, rho_bar=1.0, c_bar=1.0, vtrace_lam=1.0):
+    """One estimator call of the baseline on env-major inputs (the input
+    dicts of the sweep); returns its outputs as a tuple."""
+    import torch
+    r = x.get("rewards")
+    ref = r if r is not None else x.get("x_f32")
+    E = ref.shape[0]
+    zero_e = torch.zeros(E, dtype=torch.float32, device=ref.device)
+    boot = x.get("bootstrap") if x.get("bootstrap") is not None else zero_e
+    tv = x.get("trunc_value")
+    if kind in ("elig", "psum"):
+        xs = x["x_f32"] if kind == "elig" else x["x_i32"]
+        tm, tr = x.get("terminated"), x.get("truncated")
+        d = tm.bool() if tm is not None else torch.zeros_like(xs, dtype=torch.bool)
+        if tr is not None:
+            d = d | tr.bool()
+        first = torch.ones_like(d[..., :1])
+        keep = ~torch.cat([first, d[..., :-1]], -1)  # no edge just before t
+        beta = keep.to(xs.dtype) * (gamma * lam if kind == "elig" else 1)
+        return (torch_doubling_scan(xs, beta, reverse=False),)
+    tr, cont, end = _torch_edges(r, x.get("terminated"), x.get("truncated"))
+    tvt = torch.where(tr, tv, torch.zeros_like(r)) if tv is not None else torch.zeros_like(r)
+    bend = end * boot[:, None]
+    if kind == "retrace":
+        q, pi = x["q"], x["pi"]
+        ev = (pi * q).sum(-1)
+        a = x["actions"].long()[..., None]
+        qa = torch.gather(q, -1, a)[..., 0]
+        c = lam * torch.clamp(torch.gather(pi, -1, a)[..., 0] / x["mu_a"], max=1.0)
+        ev_n, qa_n, c_n = (_torch_next(t, zero_e) for t in (ev, qa, c))
+        alpha = r + gamma * (tvt + bend + cont * (ev_n - c_n * qa_n))
+        return (torch_doubling_scan(alpha, gamma * c_n * cont),)
+    v = x["values"]
+    v_n = _torch_next(v, zero_e)
+    nv = tvt + bend + cont * v_n  # successor value (0 where terminated)
+    if kind == "vtrace":
+        ratio = torch.exp(x["logp_target"] - x["logp_behaviour"])
+        rho = torch.clamp(ratio, max=rho_bar)
+        c = vtrace_lam * torch.clamp(ratio, max=c_bar)
+        dvs = torch_doubling_scan(rho * (r + gamma * nv - v), gamma * c * cont)
+        vs = v + dvs
+        nvs = tvt + bend + cont * _torch_next(vs, zero_e)
+        return vs, rho * (r + gamma * nvs - v)
+    outs = []
+    if kind in ("gae", "vt"):
+        adv = torch_doubling_scan(r + gamma * nv - v, gamma * lam * cont)
+        outs += [adv, adv + v]
+    if kind in ("disc", "vt"):
+        outs.append(torch_doubling_scan(r + gamma * nv - gamma * cont * v_n, gamma * cont))
+    if kind in ("td", "vt"):
+        outs.append(torch_doubling_scan(r + gamma * (nv - lam * cont * v_n), gamma * lam * cont))
+    return tuple(outs)
+
+
+# the configurations of the paper's comparison this baseline is timed on:
+# the fused value targets / single estimators at 4096 x 128 (with
+# truncation), V-Trace at 4096 x 256, Retrace at 1024 x 2048 (A = 18)
+TORCH_BASELINE_CASES = [("vt", 4096, 128, True), ("gae", 4096, 128, True), ("disc", 4096, 128, True),
+                        ("td", 4096, 128, True), ("vtrace", 4096, 256, False), ("retrace", 1024, 2048, False),
+                        ("elig", 4096, 128, True), ("psum", 4096, 128, True)]
+TORCH_COMPILE_KINDS = tuple(c[0] for c in TORCH_BASELINE_CASES)
+
+
+def run_torch_baseline(args):
+    """One JSON line per case: device time per call of this library and of
+    the PyTorch doubling-scan baseline (eager ops captured in a CUDA graph;
+    torch.compile of the same function where it builds), on the same
+    replicas (footprint > 3 x L2), and the largest
+    difference between the two results relative to (1 + |ours|)."""
+    import torch
+    from first_order_linear_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    stream = torch.cuda.Stream(dev)
+    for kind, E, T, trunc in TORCH_BASELINE_CASES:
+        d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
+        foot = sum(v.numel() * v.element_size() for v in d.values() if isinstance(v, torch.Tensor))
+        nb = max(2, min(64, math.ceil(3 * l2 / foot)))
+        reps = [({k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()},
+                 [torch.empty(sh, dtype=dt, device=dev) for sh, dt in spec]) for _ in range(nb)]
+
+        def timed(fn):
+            with torch.cuda.stream(stream):
+                for x, o in reps[:2]:
+                    fn(x, o)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for x, o in reps:
+                    fn(x, o)
+            us = _graph_us(g, nb, stream, replays=max(3, min(50, int(20000 / max(1.0, _graph_us(g, nb, stream, 1) * nb)))))
+            del g
+            return us
+
+        ours = timed(lambda x, o: _sweep_call(kind, x, o, False))
+        eager = timed(lambda x, o: torch_doubling(kind, x))
+        with torch.cuda.stream(stream):
+            _sweep_call(kind, reps[0][0], reps[0][1], False)
+            base = torch_doubling(kind, reps[0][0])
+        stream.synchronize()
+        diff = max(float(((b.double() - a.double()).abs() / (1 + a.double().abs())).max())
+                   for a, b in zip(reps[0][1], base))
+        comp, comp_err = None, None
+        if kind in TORCH_COMPILE_KINDS and not args.skip_torch_compile:
+            try:
+                fn = torch.compile(lambda x: torch_doubling(kind, x), dynamic=False)
+                comp = timed(lambda x, o: fn(x))
+            except Exception as exc:  # noqa: BLE001 - reported, not fatal
+                comp_err = f"{type(exc).__name__}: {str(exc).splitlines()[0][:160] if str(exc) else ''}"
+        line = {"torch_doubling": kind, "E": E, "T": T, "trunc": trunc, "layout": "env-major",
+                "us_per_call_ours": round(ours, 3), "us_per_call_torch_eager": round(eager, 3),
+                "speedup_vs_eager": round(eager / ours, 2),
+                "us_per_call_torch_compile": None if comp is None else round(comp, 3),
+                "speedup_vs_compile": None if comp is None else round(comp / ours, 2),
+                "max_rel_diff": diff, "replicas": nb, "algorithmic_bytes": nbytes}
+        if comp_err:
+            line["torch_compile_error"] = comp_err
+        print(json.dumps(line), flush=True)
+        del reps, d
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_ncu_case(args):
     """Four calls of one estimator on one seeded batch and nothing else: the
     command line ncu captures (``--ncu-case vt,4096,128,em`` -> launches 0..3,
@@ -706,6 +878,9 @@ def main():
                                                     "to this CSV file")
     ap.add_argument("--sweep-dtype", choices=["f32", "bf16"], default="f32",
                     help="storage of the float arrays in --sweep (bf16: RLCA_BF16, float32 arithmetic)")
+    ap.add_argument("--torch-baseline", action="store_true",
+                    help="time the vectorised PyTorch doubling-scan baseline beside this library")
+    ap.add_argument("--skip-torch-compile", action="store_true", help="with --torch-baseline: eager only")
     ap.add_argument("--ncu-case", default="",
                     help="KIND,E,T,em|tm[,bf16]: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()
@@ -715,6 +890,8 @@ def main():
         return run_ncu_case(args)
     if args.sweep:
         return run_sweep(args)
+    if args.torch_baseline:
+        return run_torch_baseline(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -129,18 +129,17 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   Plan q = {};
   q.time_major = (flags & RLCA_TIME_MAJOR) != 0;
   const bool bf16_io = (flags & RLCA_BF16) != 0;
-  q.staged = kStagedPath && vec && !q.time_major && !retrace && !bf16_io && T % 4 == 0;
-  if (q.staged) {
-    int W = (int)std::min<int64_t>(next_pow2((T + kEsSteps - 1) / kEsSteps), kEsMaxWidth);
-    if (flags & RLCA_MULTIPASS) W = std::max(1, W / 4);
-    q.width = W;
-    q.block = std::max(W, kEsMinBlock);
-    q.rows_per_cta = q.block / W;
-    q.tile = kEsSteps * W;
-    q.smem_driver_bound = 0;  // sized by the launcher; at most ~90 KB
-    q.smem = 0;
-  } else if (q.time_major) {
-    const int cmax = retrace ? kRetraceTmMaxWidth : kTmMaxWidth;
+  if (q.time_major) {
+    // Retrace: 8 chunk warps keep two CTAs' staging buffers on an SM; 16
+    // where the environments give at most one CTA per SM anyway -- unless
+    // rows of more than one 128-step tile would, at 8, split into two-pass
+    // segments (more CTAs), a split the wider CTAs would no longer take
+    int cmax = kTmMaxWidth;
+    if (retrace) {
+      const int64_t rb = (E + 31) / 32;
+      const bool c8_splits = T > 64 && 16 * rb * 256 < (int64_t)sm_count * 1024;
+      cmax = rb <= sm_count && (!c8_splits || T <= 128) ? kRetraceTmMaxWidth : kRetraceTmMaxWidth / 2;
+    }
     int C = (int)std::min<int64_t>(next_pow2((T + 7) / 8), cmax);
     if (flags & RLCA_MULTIPASS) C = std::max(1, C / 4);
     // Retrace's per-warp staging grows with A: fewer chunk warps when it would not fit
@@ -189,7 +188,7 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   // one affine map per (row, segment): two values, two of each for the fused value targets
   const size_t ws_elem = kind == Kind::ValueTargets ? 16 : 8;
   q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
-  const bool fast_ok = !q.staged && !q.time_major && vec && q.nseg == 1 && !(flags & RLCA_MULTIPASS);
+  const bool fast_ok = !q.time_major && vec && q.nseg == 1 && !(flags & RLCA_MULTIPASS);
   q.fast = fast_ok && T % kEmSteps == 0 && q.ntiles == 1;
   q.steps = kEmSteps;
   // 8 steps a thread (half the warps and scan rounds a row) where the

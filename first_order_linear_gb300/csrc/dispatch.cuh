@@ -162,16 +162,6 @@ static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, c
   return cudaErrorInvalidConfiguration;
 }
 
-template <class Est, int W>
-static cudaError_t launch_es_w(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
-  if constexpr (kStagedPath && Est::kStageable && W <= kEsMaxWidth &&
-                std::is_same<typename Est::Store, float>::value) {
-    return launch_one<Est>(es_scan_kernel<Est, W>, p, es_smem_bytes<Est, W>(), est, g, s);
-  } else {
-    return cudaErrorInvalidConfiguration;
-  }
-}
-
 template <class Est>
 static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if (p.fast) {
@@ -187,20 +177,6 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
       case 256: return launch_fast_w<Est, 256>(p, est, g, s);
       case 512: return launch_fast_w<Est, 512>(p, est, g, s);
       case 1024: return launch_fast_w<Est, 1024>(p, est, g, s);
-      default: return cudaErrorInvalidConfiguration;
-    }
-  }
-  if (p.staged) {
-    switch (p.width) {
-      case 1: return launch_es_w<Est, 1>(p, est, g, s);
-      case 2: return launch_es_w<Est, 2>(p, est, g, s);
-      case 4: return launch_es_w<Est, 4>(p, est, g, s);
-      case 8: return launch_es_w<Est, 8>(p, est, g, s);
-      case 16: return launch_es_w<Est, 16>(p, est, g, s);
-      case 32: return launch_es_w<Est, 32>(p, est, g, s);
-      case 64: return launch_es_w<Est, 64>(p, est, g, s);
-      case 128: return launch_es_w<Est, 128>(p, est, g, s);
-      case 256: return launch_es_w<Est, 256>(p, est, g, s);
       default: return cudaErrorInvalidConfiguration;
     }
   }

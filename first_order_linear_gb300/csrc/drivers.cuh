@@ -1,6 +1,7 @@
-// drivers.cuh -- the scan kernels: direct env-major, time-major, and the
-// shared-memory-staged env-major driver.  See scan_core.cuh for the scan
-// structure they share and estimators.cuh for the estimator interface.
+// drivers.cuh -- the scan kernels: env-major (general and one-tile fast),
+// time-major (general, fast, and staged through a shared-memory ring).  See
+// scan_core.cuh for the scan structure they share and estimators.cuh for the
+// estimator interface.
 #pragma once
 
 #include "estimators.cuh"
@@ -761,216 +762,6 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
   }
   if (agg_mode && cs == 0 && row0 + js < g.E)
     reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
-}
-
-// ---------------------------------------------------------------------------
-// staged env-major driver
-//
-// For 16-byte aligned env-major rows (T % 4 == 0).  Each tile of the CTA's
-// rows is copied into shared memory with coalesced 16-byte async copies (4
-// bytes for flags), each thread reads its SL consecutive steps from a padded
-// slot, scans as in em_scan_kernel, writes its outputs back into the same
-// float buffers, and the CTA copies them out with coalesced 16-byte stores.
-// Thread slot s = tid holds steps [t0, t0 + SL) of row row0 + tid / TPR.
-// ---------------------------------------------------------------------------
-template <class Est>
-__host__ __device__ constexpr int es_float_buffers() {
-  return Est::kSF > Est::kSO ? Est::kSF : Est::kSO;
-}
-template <class Est, int TPR>
-__host__ __device__ constexpr size_t es_xw_bytes() {
-  using S = EsShape<TPR>;
-  return S::NWR > 1 ? align16((size_t)2 * S::ROWS * S::NWR * sizeof(Aff<typename Est::V>)) : 0;
-}
-template <class Est, int TPR>
-__host__ __device__ constexpr size_t es_smem_bytes() {
-  using S = EsShape<TPR>;
-  return es_xw_bytes<Est, TPR>() + (size_t)es_float_buffers<Est>() * S::FSTRIDE * 4 + (size_t)Est::kSB * S::BSTRIDE;
-}
-
-template <class Est, int TPR>
-__global__ void __launch_bounds__(EsShape<TPR>::BLOCK)
-    es_scan_kernel(Est est, Geom g) {
-  using S = EsShape<TPR>;
-  using V = typename Est::V;
-  constexpr bool BWD = Est::kBackward;
-  constexpr int L = S::L, GW = S::GW, NWR = S::NWR;
-  constexpr int QPR = S::TILE / 4;  // 4-element chunks per row of a tile
-  constexpr int QPT = L / 4;        // chunks per thread slot
-
-  extern __shared__ __align__(16) unsigned char smem[];
-  Aff<V>* xw = reinterpret_cast<Aff<V>*>(smem);
-  float* fbuf = reinterpret_cast<float*>(smem + es_xw_bytes<Est, TPR>());
-  uint8_t* bbuf = reinterpret_cast<uint8_t*>(fbuf + es_float_buffers<Est>() * S::FSTRIDE);
-
-  const int tid = threadIdx.x;
-  const int j = tid % TPR;
-  const int rloc = tid / TPR;
-  const int lane = tid & 31;
-  const int lig = j % GW;
-  const int wr = j / 32;
-  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
-  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * S::ROWS;
-  const int64_t row = row0 + rloc;
-  const bool row_ok = row < g.E;
-  const int seg_lo = seg * g.seg_len;
-  const int seg_hi = min(g.T, seg_lo + g.seg_len);
-  const bool agg_mode = g.mode == kModeAggregate;
-  const EnvMajor lay{g.E, g.T};
-  const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
-  if (!early) pdl_wait();
-
-  StagedList lst;
-  est.staged_io(lst);
-
-  Aff<V> carry;
-  if (agg_mode) {
-    carry = aff_identity<V>();
-  } else {
-    V c0 = row_ok ? est.row_carry(row) : V(0);
-    if (g.nseg > 1 && row_ok) c0 = segment_carry_in<V, BWD>(g, row, seg, c0);
-    carry = {c0, V(0)};
-  }
-
-  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
-  for (int it = 0; it < ntiles; ++it) {
-    const int tile = BWD ? ntiles - 1 - it : it;
-    const int ts = seg_lo + tile * S::TILE;
-    const int te = min(seg_hi, ts + S::TILE);
-    const int t0 = ts + j * L;
-    const int n = row_ok ? max(0, min(L, te - t0)) : 0;
-    const int span4 = (te - ts) >> 2;  // te - ts is a multiple of 4 on this path
-
-    if (it > 0) __syncthreads();  // the previous tile's copy-out has read the buffers
-    // stage the tile: chunk c = (row r of the CTA, 4-step chunk q of the tile)
-#pragma unroll
-    for (int c0 = 0; c0 < S::CHUNKS; c0 += S::BLOCK) {
-      const int c = c0 + tid;
-      const int r = c / QPR, q = c % QPR;
-      const int64_t grow = row0 + r;
-      if (c < S::CHUNKS && grow < g.E && q < span4) {
-        const int64_t ge = grow * (int64_t)g.T + ts + 4 * q;
-        const int doff = (r * TPR + q / QPT) * S::PAD + (q % QPT) * 4;
-#pragma unroll
-        for (int b = 0; b < Est::kSF; ++b)
-          cp_async16(fbuf + b * S::FSTRIDE + doff, static_cast<const float*>(lst.fin[b]) + ge);
-#pragma unroll
-        for (int b = 0; b < Est::kSB; ++b)
-          if (lst.bin[b] != nullptr) cp_async4(bbuf + b * S::BSTRIDE + r * S::TILE + 4 * q, lst.bin[b] + ge);
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-
-    typename Est::template Regs<L> R;
-    const SIO<L> io{fbuf, bbuf, S::FSTRIDE, S::BSTRIDE, tid, lay, row, t0, n};
-    est.template load<L>(R, io, rloc, ts, S::TILE, S::ROWS, nullptr);
-    if (it == ntiles - 1) pdl_trigger();
-    __syncthreads();  // every slot is in registers: the float buffers may take outputs
-
-    if constexpr (Est::kNb > 0) {
-      float give[Est::kNb > 0 ? Est::kNb : 1], got[Est::kNb > 0 ? Est::kNb : 1];
-      est.nb_give(R, give);
-#pragma unroll
-      for (int i = 0; i < Est::kNb; ++i)
-        got[i] = BWD ? __shfl_down_sync(kFullMask, give[i], 1, GW) : __shfl_up_sync(kFullMask, give[i], 1, GW);
-      const int tn = BWD ? t0 + L : t0 - 1;
-      const bool edge = BWD ? (lig == GW - 1 || t0 + L >= te) : (lig == 0);
-      if (n > 0 && edge && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
-      est.nb_take(R, got);
-    }
-
-    Aff<V> c[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) c[k] = (k < n) ? est.coef(R, k, t0 + k) : aff_identity<V>();
-    Aff<V> agg = aff_identity<V>();
-    if (BWD) {
-#pragma unroll
-      for (int k = L - 1; k >= 0; --k) agg = compose(c[k], agg);
-    } else {
-#pragma unroll
-      for (int k = 0; k < L; ++k) agg = compose(c[k], agg);
-    }
-    Aff<V> inc = agg;
-#pragma unroll
-    for (int off = 1; off < GW; off <<= 1) {
-      if (BWD) {
-        Aff<V> o = shfl_down_aff(inc, off, GW);
-        if (lig + off < GW) inc = compose(inc, o);
-      } else {
-        Aff<V> o = shfl_up_aff(inc, off, GW);
-        if (lig >= off) inc = compose(inc, o);
-      }
-    }
-    Aff<V> exc = BWD ? shfl_down_aff(inc, 1, GW) : shfl_up_aff(inc, 1, GW);
-    if (lig == (BWD ? GW - 1 : 0)) exc = aff_identity<V>();
-
-    Aff<V> boundary, next_carry;
-    if constexpr (NWR > 1) {
-      Aff<V>* x = xw + ((it & 1) * S::ROWS + rloc) * NWR;
-      if (lane == (BWD ? 0 : 31)) x[wr] = inc;
-      __syncthreads();
-      Aff<V> tw = lane < NWR ? x[lane] : aff_identity<V>();
-#pragma unroll
-      for (int off = 1; off < NWR; off <<= 1) {
-        if (BWD) {
-          Aff<V> o = shfl_down_aff(tw, off, 32);
-          if (lane + off < NWR) tw = compose(tw, o);
-        } else {
-          Aff<V> o = shfl_up_aff(tw, off, 32);
-          if (lane >= off) tw = compose(tw, o);
-        }
-      }
-      const int src = BWD ? wr + 1 : wr - 1;
-      Aff<V> ex = shfl_idx_aff(tw, src & 31, 32);
-      if (BWD ? (wr == NWR - 1) : (wr == 0)) ex = aff_identity<V>();
-      boundary = compose(ex, carry);
-      next_carry = compose(shfl_idx_aff(tw, BWD ? 0 : NWR - 1, 32), carry);
-    } else {
-      boundary = carry;
-      Aff<V> tot = shfl_idx_aff(inc, BWD ? 0 : GW - 1, GW);
-      next_carry = compose(tot, carry);
-    }
-
-    if (!agg_mode) {
-      V A = compose(exc, boundary).a;
-      if (BWD) {
-#pragma unroll
-        for (int k = L - 1; k >= 0; --k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          V adj = A;
-          A = c[k].a + c[k].b * A;
-          est.emit(R, k, A, adj, c[k]);
-        }
-      }
-      est.template store<L>(R, io);  // into the float buffers
-      __syncthreads();
-      if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
-#pragma unroll
-      for (int c0 = 0; c0 < S::CHUNKS; c0 += S::BLOCK) {
-        const int cc = c0 + tid;
-        const int r = cc / QPR, q = cc % QPR;
-        const int64_t grow = row0 + r;
-        if (cc < S::CHUNKS && grow < g.E && q < span4) {
-          const int64_t ge = grow * (int64_t)g.T + ts + 4 * q;
-          const int doff = (r * TPR + q / QPT) * S::PAD + (q % QPT) * 4;
-#pragma unroll
-          for (int b = 0; b < Est::kSO; ++b)
-            if (lst.out[b] != nullptr)
-              *reinterpret_cast<float4*>(static_cast<float*>(lst.out[b]) + ge) =
-                  *reinterpret_cast<const float4*>(fbuf + b * S::FSTRIDE + doff);
-        }
-      }
-    }
-    carry = next_carry;
-  }
-  if (agg_mode && row_ok && j == 0) reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
 }
 
 }  // namespace rlca

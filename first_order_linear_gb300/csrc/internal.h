@@ -17,13 +17,12 @@ enum class Kind { Gae, Disc, TdLambda, Vtrace, Retrace, Elig, PrefixSum, Affine,
 constexpr int kEmMaxWidth = 1024;
 constexpr int kTmMaxWidth = 32;
 constexpr int kRetraceEmMaxWidth = 256;
-constexpr int kRetraceTmMaxWidth = 8;
+constexpr int kRetraceTmMaxWidth = 16;
 constexpr int kEmMinWidth = 1;
 constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 struct Plan {
   bool time_major;
-  bool staged;      // env-major tiles staged through shared memory (es_scan_kernel)
   bool fast;        // env-major, one tile per row, one segment (em_fast_kernel)
   bool tm_fast;     // time-major, T % 8 == 0, E * T < 2^32, one segment (tm_fast_kernel)
   bool tm_staged;   // ... and inputs staged through shared memory (tm_staged_kernel)
@@ -59,13 +58,6 @@ constexpr bool kTmStaged = RLCA_TM_STAGED != 0;
 // ... also for float32 tiles of 16 environments (rows of 64 bytes) where the
 // direct driver would take 8
 constexpr bool kTmStaged16 = RLCA_TM_STAGED16 != 0;
-
-#ifndef RLCA_STAGED_PATH
-#define RLCA_STAGED_PATH 0
-#endif
-// build-time choice: env-major tiles staged through shared memory
-// (es_scan_kernel) instead of the register drivers
-constexpr bool kStagedPath = RLCA_STAGED_PATH != 0;
 
 // Launches the scan of one estimator functor (both passes of the two-pass
 // path when p.nseg > 1).  Defined by explicit instantiation in the family

@@ -344,32 +344,6 @@ struct EmShape {
   static constexpr int NWR = TPR > 32 ? TPR / 32 : 1;  // warps per row
 };
 
-// staged env-major (shared-memory tiles): TPR threads per row, SL steps per
-// thread, rows packed kEsMinBlock threads per CTA
-#ifndef RLCA_ES_STEPS
-#define RLCA_ES_STEPS 16
-#endif
-#ifndef RLCA_ES_MIN_BLOCK
-#define RLCA_ES_MIN_BLOCK 128
-#endif
-constexpr int kEsSteps = RLCA_ES_STEPS;
-constexpr int kEsMinBlock = RLCA_ES_MIN_BLOCK;
-constexpr int kEsMaxWidth = 256;
-
-template <int TPR>
-struct EsShape {
-  static constexpr int L = kEsSteps;
-  static constexpr int TILE = TPR * L;
-  static constexpr int BLOCK = TPR >= kEsMinBlock ? TPR : kEsMinBlock;
-  static constexpr int ROWS = BLOCK / TPR;
-  static constexpr int GW = TPR < 32 ? TPR : 32;
-  static constexpr int NWR = TPR > 32 ? TPR / 32 : 1;
-  static constexpr int PAD = L + 4;            // floats per thread slot in a float buffer
-  static constexpr int FSTRIDE = BLOCK * PAD;  // floats per float buffer
-  static constexpr int BSTRIDE = BLOCK * L;    // bytes per flag buffer
-  static constexpr int CHUNKS = ROWS * TILE / 4;  // 4-element chunks per CTA tile
-};
-
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // async global -> shared copies (completed by cp_async_wait_all, a hardware
