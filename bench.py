@@ -302,6 +302,22 @@ def _graph_us(g, launches, stream, replays=20):
     return a.elapsed_time(b) * 1e3 / (replays * launches)
 
 
+def _full_call_us(fn, items, stream, n=200):
+    """Host wall time per call of ``fn(item)`` issued back to back in plain
+    stream order (argument checks, marshalling and launch included, one
+    synchronisation at each end): the full-call time, as a caller sees it."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(min(5, n)):
+            fn(items[i % len(items)])
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n):
+            fn(items[i % len(items)])
+        stream.synchronize()
+    return (time.perf_counter() - t0) / n * 1e6
+
+
 def run_ours(args):
     import torch
 
@@ -392,6 +408,16 @@ def run_ours(args):
                       "env_steps_per_s_per_estimator": (N_EST if len(fns) != 1 or name.startswith("value") else 1)
                       * E * T / (us / 1e6)}
         del g
+    # the public Python call (rlca.rlca_value_targets), launches in plain
+    # stream order without graphs: host wall time per call
+    from first_order_linear_gb300 import rlca
+
+    def api_call(x):
+        rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
+                                x["bootstrap"], gamma=GAMMA, lambda_=LAMBDA, advantages=x["adv"], returns=x["ret"],
+                                disc_returns=x["disc"], td_lambda_returns=x["td"], inputs_ready=True, stream=stream)
+    kern["value_targets_full_call"] = {"us_per_call": _full_call_us(api_call, reps, stream),
+                                       "timing": "host wall clock over 200 back-to-back public-API calls"}
     n_trunc = int(d_cpu["truncated"].sum())
     fused_bytes = E * T * (4 + 4 + 1 + 1 + 4 * 4) + 32 * n_trunc + 4 * E
     peak, peak_kind = _peaks()
@@ -782,8 +808,9 @@ def run_torch_baseline(args):
     """One JSON line per case: device time per call of this library and of
     the PyTorch doubling-scan baseline (eager ops captured in a CUDA graph;
     torch.compile of the same function where it builds), on the same
-    replicas (footprint > 3 x L2), and the largest
-    difference between the two results relative to (1 + |ours|)."""
+    replicas (footprint > 3 x L2); the full-call (host wall) time per call of
+    each in plain stream order; and the largest difference between the two
+    results relative to (1 + |ours|)."""
     import torch
     from first_order_linear_gb300 import build
     build.build()
@@ -819,11 +846,14 @@ def run_torch_baseline(args):
         stream.synchronize()
         diff = max(float(((b.double() - a.double()).abs() / (1 + a.double().abs())).max())
                    for a, b in zip(reps[0][1], base))
-        comp, comp_err = None, None
+        full_ours = _full_call_us(lambda r: _sweep_call(kind, r[0], r[1], False), reps, stream)
+        full_eager = _full_call_us(lambda r: torch_doubling(kind, r[0]), reps, stream)
+        comp, comp_err, full_comp = None, None, None
         if kind in TORCH_COMPILE_KINDS and not args.skip_torch_compile:
             try:
                 fn = torch.compile(lambda x: torch_doubling(kind, x), dynamic=False)
                 comp = timed(lambda x, o: fn(x))
+                full_comp = _full_call_us(lambda r: fn(r[0]), reps, stream)
             except Exception as exc:  # noqa: BLE001 - reported, not fatal
                 comp_err = f"{type(exc).__name__}: {str(exc).splitlines()[0][:160] if str(exc) else ''}"
         line = {"torch_doubling": kind, "E": E, "T": T, "trunc": trunc, "layout": "env-major",
@@ -831,6 +861,9 @@ def run_torch_baseline(args):
                 "speedup_vs_eager": round(eager / ours, 2),
                 "us_per_call_torch_compile": None if comp is None else round(comp, 3),
                 "speedup_vs_compile": None if comp is None else round(comp / ours, 2),
+                "full_call_us_ours": round(full_ours, 2), "full_call_us_torch_eager": round(full_eager, 2),
+                "full_call_us_torch_compile": None if full_comp is None else round(full_comp, 2),
+                "full_call_speedup_vs_compile": None if full_comp is None else round(full_comp / full_ours, 2),
                 "max_rel_diff": diff, "replicas": nb, "algorithmic_bytes": nbytes}
         if comp_err:
             line["torch_compile_error"] = comp_err

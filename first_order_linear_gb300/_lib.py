@@ -76,6 +76,8 @@ def load() -> C.CDLL:
     """The loaded library with argument types set.  Raises RuntimeError
     when librlca.so has not been built."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):

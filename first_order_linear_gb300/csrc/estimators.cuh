@@ -24,8 +24,8 @@
 //   emit(R, k, A, adj, c)       output of step k from A_t (adj = A of the
 //                               step the recurrence reads)
 //   store(R, io)                write the thread's outputs through io
-//   kStageable, staged_io(f)    inputs / outputs the staged driver may stage
-//                               (floats, then flag bytes, then outputs)
+//   kStageable, staged_io(f)    inputs the staged driver may stage (floats,
+//                               then flag bytes)
 #pragma once
 
 #include <type_traits>
@@ -106,14 +106,12 @@ struct GaeEst : NoStage {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 2, kSB = 2, kSO = 2;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
-    f.out_f(adv);
-    f.out_f(ret);
   }
   BoundaryArgs b;
   const float* r;
@@ -175,12 +173,11 @@ struct DiscEst : NoStage {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     staged_flags(b, f);
-    f.out_f(out);
   }
   BoundaryArgs b;
   const float* r;
@@ -234,13 +231,12 @@ struct TdLambdaEst : NoStage {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 2, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
-    f.out_f(out);
   }
   BoundaryArgs b;
   const float* r;
@@ -306,16 +302,12 @@ struct ValueTargetsEst : NoStage {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 2, kSB = 2, kSO = 4;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
-    f.out_f(adv);
-    f.out_f(ret);
-    f.out_f(disc);
-    f.out_f(td);
   }
   BoundaryArgs b;
   const float* r;
@@ -390,7 +382,7 @@ struct VtraceEst : NoStage {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 4, kSB = 2, kSO = 2;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 4, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
@@ -398,8 +390,6 @@ struct VtraceEst : NoStage {
     f.in_f(lpt);
     f.in_f(lpb);
     staged_flags(b, f);
-    f.out_f(vs);
-    f.out_f(pg);
   }
   BoundaryArgs b;
   const float* r;
@@ -646,7 +636,7 @@ struct RetraceEst {
   static constexpr bool kBackward = true;
   static constexpr int kNb = 0;
   static constexpr bool kStageable = false;
-  static constexpr int kSF = 0, kSB = 0, kSO = 0;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 0, kSB = 0;  // staged float inputs, flag inputs
   BoundaryArgs b;
   RetraceStage<ST> st;
   const float* r;
@@ -775,13 +765,12 @@ struct EligEst : NoStage {
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(x);
     f.in_b(term);
     f.in_b(trunc);
-    f.out_f(out);
   }
   const float* x;
   const uint8_t* term;   // nullable
@@ -842,13 +831,12 @@ struct PrefixSumEst : NoStage {
   static constexpr bool kBackward = false;
   static constexpr int kNb = 1;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 1, kSB = 2, kSO = 1;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(x);
     f.in_b(term);
     f.in_b(trunc);
-    f.out_f(out);
   }
   const void* x;
   const uint8_t* term;
@@ -917,12 +905,11 @@ struct AffineEst : NoStage {
   static constexpr bool kBackward = BWD;
   static constexpr int kNb = 0;
   static constexpr bool kStageable = true;
-  static constexpr int kSF = 2, kSB = 0, kSO = 1;  // staged float inputs, flag inputs, outputs
+  static constexpr int kSF = 2, kSB = 0;  // staged float inputs, flag inputs
   template <class F>
   __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(alpha);
     f.in_f(beta);
-    f.out_f(out);
   }
   const float* alpha;
   const float* beta;

@@ -151,16 +151,14 @@ struct TmSIO {
   }
 };
 
-// Collects an estimator's staged inputs and outputs (in staged_io order).
+// Collects an estimator's staged inputs (in staged_io order).
 struct StagedList {
-  static constexpr int kMaxF = 4, kMaxB = 2, kMaxO = 4;
+  static constexpr int kMaxF = 4, kMaxB = 2;
   const void* fin[kMaxF];
   const uint8_t* bin[kMaxB];
-  void* out[kMaxO];
-  int nf = 0, nb = 0, no = 0;
+  int nf = 0, nb = 0;
   __device__ __forceinline__ void in_f(const void* p) { fin[nf++] = p; }
   __device__ __forceinline__ void in_b(const uint8_t* p) { bin[nb++] = p; }
-  __device__ __forceinline__ void out_f(void* p) { out[no++] = p; }
 };
 
 }  // namespace rlca

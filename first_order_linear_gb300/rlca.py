@@ -29,13 +29,18 @@ __all__ = [
 
 
 def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    # a plain int: the entry points' argtypes turn it into a void*
+    return None if t is None else t.data_ptr()
 
 
 def _check(t, name, dtypes, shape, device, required=True):
     if t is None:
         if required:
             raise ValueError(f"{name} is required")
+        return
+    # one combined test on the common path; the detailed checks name the fault
+    if (isinstance(t, torch.Tensor) and t.dtype in dtypes and t.shape == shape and t.device == device
+            and t.is_contiguous()):
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -80,14 +85,25 @@ def _dims(x, time_major):
     return (x.shape[1], x.shape[0]) if time_major else (x.shape[0], x.shape[1])
 
 
+# workspace sizes by (estimator, E, T, A, flags, device index): a size
+# depends only on these and the device's SM count, so each is asked once
+_ws_sizes = {}
+
+
 def rlca_workspace_size(estimator: int, E: int, T: int, num_actions: int = 0, flags: int = 0,
                         device=None) -> int:
     """Bytes of workspace a call needs on ``device`` (default: current)."""
-    lib = _lib.load()
-    out = C.c_size_t(0)
-    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        check("rlca_workspace_size", lib.rlca_workspace_size(estimator, E, T, num_actions, flags, C.byref(out)))
-    return out.value
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    index = dev.index if dev.index is not None else torch.cuda.current_device()
+    key = (estimator, E, T, num_actions, flags, index)
+    need = _ws_sizes.get(key)
+    if need is None:
+        lib = _lib.load()
+        out = C.c_size_t(0)
+        with torch.cuda.device(index):
+            check("rlca_workspace_size", lib.rlca_workspace_size(estimator, E, T, num_actions, flags, C.byref(out)))
+        need = _ws_sizes[key] = out.value
+    return need
 
 
 def _workspace(estimator, E, T, A, flags, device, workspace):
@@ -103,7 +119,7 @@ def _workspace(estimator, E, T, A, flags, device, workspace):
 
 def _stream(device, stream):
     s = stream if stream is not None else torch.cuda.current_stream(device)
-    return C.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F=_F):
