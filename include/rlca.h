@@ -307,8 +307,10 @@ int rlca_vtrace(const float *rewards, const float *values,
  * (trunc_value: E_pi Q of the truncated episode's last state; bootstrap:
  * E_pi Q of the state after the window).  The action dimension is reduced
  * per step on chip before the scan, so registers do not grow with T.
- *   q, pi        [E,T,A] f32 (A = num_actions fastest), required
- *   mu_a         [E,T] f32 behaviour probability of the taken action (> 0)
+ *   q, pi        [E,T,A] f32, or bf16 with RLCA_BF16 (A = num_actions
+ *                fastest), required
+ *   mu_a         [E,T] f32 (bf16 with RLCA_BF16) behaviour probability of
+ *                the taken action (> 0)
  *   actions      [E,T] int32 in [0, A); values outside are clamped into
  *                range (memory-safe, result unspecified)
  *   q_ret        [E,T] f32 output, required
