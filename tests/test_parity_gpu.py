@@ -222,6 +222,19 @@ def test_retrace_action_counts(A):
         parity.check_case("retrace", 24, 160, seed=A, time_major=tm, num_actions=A, p_term=0.02)
 
 
+def test_retrace_time_major_widths():
+    """Time-major Retrace at each staging width: 16 chunk warps (128-step
+    tiles) where the environments give at most one CTA per SM, 8 beyond
+    that, 8 with two-pass segments for few environments with long rows,
+    and fewer where many actions fill the staging buffers; float32 and
+    bfloat16."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cases = [(32 * sms, 512, 18), (32 * sms + 32, 256, 18), (1024, 1024, 18), (32 * sms, 256, 64)]
+    for i, (E, T, A) in enumerate(cases):
+        for bf16 in (False, True):
+            parity.check_case("retrace", E, T, seed=70 + i, time_major=True, num_actions=A, bf16=bf16)
+
+
 def test_vtrace_clipping_and_lambda():
     p = dict(rho_bar=1.3, c_bar=0.7, vt_lambda=0.9)
     for tm in (False, True):
