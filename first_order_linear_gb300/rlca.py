@@ -98,6 +98,8 @@ def rlca_workspace_size(estimator: int, E: int, T: int, num_actions: int = 0, fl
     key = (estimator, E, T, num_actions, flags, index)
     need = _ws_sizes.get(key)
     if need is None:
+        if len(_ws_sizes) >= 4096:  # many distinct shapes: start over rather than grow without bound
+            _ws_sizes.clear()
         lib = _lib.load()
         out = C.c_size_t(0)
         with torch.cuda.device(index):
