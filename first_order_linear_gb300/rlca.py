@@ -1,9 +1,11 @@
 """PyTorch-facing wrappers of the C ABI, one per entry point, same names.
 
 Each wrapper checks dtypes, devices and contiguity, allocates the outputs
-(unless given) and the two-pass workspace, and makes exactly one call into
-``librlca.so`` on the current CUDA stream.  No arithmetic of the method runs
-here; a missing library raises (see :func:`first_order_linear_gb300._lib.load`).
+(unless given) and the two-pass workspace, and makes one entry-point call
+into ``librlca.so`` on the current CUDA stream (plus, the first time a shape
+is seen, a workspace-size query whose answer is kept).  No arithmetic of
+the method runs here; a missing library raises (see
+:func:`first_order_linear_gb300._lib.load`).
 
 Layout: env-major ``[E, T]`` by default; ``time_major=True`` takes ``[T, E]``
 (and ``[T, E, A]`` for Retrace's per-action tensors).  ``inputs_ready=True``
