@@ -30,6 +30,14 @@ __all__ = [
 ]
 
 
+def _require_cuda(dev):
+    """The call's tensors (all on ``dev`` by the checks before) must be on a
+    CUDA device: the kernels read device memory and there is no host
+    implementation."""
+    if dev.type != "cuda":
+        raise ValueError(f"tensors are on {dev}: the kernels need tensors on a CUDA device")
+
+
 def _ptr(t):
     # a plain int: the entry points' argtypes turn it into a void*
     return None if t is None else t.data_ptr()
@@ -155,6 +163,7 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
     _check(advantages, "advantages", F, shape, dev)
     _check(returns, "returns", F, shape, dev, required=False)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_GAE, E, T, 0, flags, dev, workspace)
         check("rlca_gae", lib.rlca_gae(
@@ -188,6 +197,7 @@ def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_v
             bufs[name] = torch.empty(shape, dtype=fdt, device=dev)
         _check(bufs[name], name, F, shape, dev, required=False)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VALUE_TARGETS, E, T, 0, flags, dev, workspace)
         check("rlca_value_targets", lib.rlca_value_targets(
@@ -213,6 +223,7 @@ def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value
         out = torch.empty(shape, dtype=fdt, device=dev)
     _check(out, "out", F, shape, dev)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_DISCOUNTED_RETURN, E, T, 0, flags, dev, workspace)
         check("rlca_discounted_return", lib.rlca_discounted_return(
@@ -238,6 +249,7 @@ def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value
         out = torch.empty(shape, dtype=fdt, device=dev)
     _check(out, "out", F, shape, dev)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_TD_LAMBDA, E, T, 0, flags, dev, workspace)
         check("rlca_td_lambda", lib.rlca_td_lambda(
@@ -268,6 +280,7 @@ def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, t
     _check(vs, "vs", F, shape, dev)
     _check(pg_advantages, "pg_advantages", F, shape, dev, required=False)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_VTRACE, E, T, 0, flags, dev, workspace)
         check("rlca_vtrace", lib.rlca_vtrace(
@@ -300,6 +313,7 @@ def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None,
         out = torch.empty(shape, dtype=fdt, device=dev)
     _check(out, "out", F, shape, dev)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_RETRACE, E, T, A, flags, dev, workspace)
         check("rlca_retrace", lib.rlca_retrace(
@@ -325,6 +339,7 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
         out = torch.empty(shape, dtype=fdt, device=dev)
     _check(out, "out", F, shape, dev)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_ELIG_TRACE, E, T, 0, flags, dev, workspace)
         check("rlca_elig_trace", lib.rlca_elig_trace(
@@ -355,6 +370,7 @@ def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=Fa
     extra = (_lib.RLCA_PSUM_EXCLUSIVE if exclusive else 0) | (_lib.RLCA_PSUM_FLAG_IS_START if flag_is_start else 0)
     flags = _flags(time_major, multipass, extra, inputs_ready=inputs_ready) | (
         _lib.RLCA_BF16 if x.dtype == torch.bfloat16 else 0)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_PREFIX_SUM, E, T, 0, flags, dev, workspace)
         check("rlca_episodic_prefix_sum", lib.rlca_episodic_prefix_sum(
@@ -379,6 +395,7 @@ def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_ma
         out = torch.empty(shape, dtype=fdt, device=dev)
     _check(out, "out", F, shape, dev)
     flags = _flags(time_major, multipass, inputs_ready=inputs_ready) | _fflag(fdt)
+    _require_cuda(dev)
     with torch.cuda.device(dev):
         ws, wsb = _workspace(_lib.RLCA_EST_AFFINE_SCAN, E, T, 0, flags, dev, workspace)
         check("rlca_affine_scan", lib.rlca_affine_scan(
