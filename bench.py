@@ -696,12 +696,13 @@ def run_sweep(args):
 
 # ---------------------------------------------------------------------------
 # The vectorised PyTorch doubling-scan baseline: the form of comparison the
-# paper quotes its speed-ups against (rl-triton (arXiv:2608.17641) §1
-# Introduction, §7 Results): each estimator's (alpha, beta) built with
-# whole-tensor torch ops, then log2(T) recursive-doubling passes of affine
-# map composition over the whole [E, T] tensor.  Env-major, float32 (int32
-# for the prefix sum).  A measurement baseline only: the library never runs
-# it.
+# paper quotes its speed-ups against (rl-triton (arXiv:2608.17641) §6
+# Benchmarking Methodology, baseline design; §7 Results): each estimator's
+# (alpha, beta) built with whole-tensor torch ops, then log2(T)
+# recursive-doubling passes of affine map composition over the whole
+# [E, T] tensor (suffix passes for the backward estimators, prefix passes
+# for the forward ones).  Env-major, float32 (int32 for the prefix sum).  A
+# measurement baseline only: the library never runs it.
 # ---------------------------------------------------------------------------
 
 def torch_doubling_scan(alpha, beta, reverse=True):
@@ -873,6 +874,58 @@ def run_torch_baseline(args):
     return 0
 
 
+# the configurations the pages name, timed as the pages time them
+PAGES_PROTOCOL_CASES = [("vt", 4096, 128, True), ("vtrace", 4096, 256, False), ("retrace", 1024, 2048, False)]
+
+
+def run_pages_protocol(args):
+    """The paper's timing protocol (rl-triton (arXiv:2608.17641) §6
+    Benchmarking Methodology) on the named configurations: 20 untimed
+    calls, then 5 trials of 50 calls, each call alone between two CUDA
+    events on its stream; the figure is the smallest of the 5 per-trial
+    medians.  Added here: L2 is flushed before each call (a memset of twice
+    the L2 size, outside the events), so the figure is one isolated launch
+    from a cold L2, nothing overlapped."""
+    import torch
+    from first_order_linear_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for kind, E, T, trunc in PAGES_PROTOCOL_CASES:
+        d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
+        o = [torch.empty(sh, dtype=dt, device=dev) for sh, dt in spec]
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                _sweep_call(kind, d, o, False)
+            stream.synchronize()
+            medians = []
+            for _ in range(5):
+                ts = []
+                for _ in range(50):
+                    flush.zero_()
+                    a.record(stream)
+                    _sweep_call(kind, d, o, False)
+                    b.record(stream)
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e3)
+                medians.append(statistics.median(ts))
+        us = min(medians)
+        print(json.dumps({"pages_protocol": kind, "E": E, "T": T, "trunc": trunc, "layout": "env-major",
+                          "us_per_call": round(us, 3), "trial_medians_us": [round(m, 3) for m in medians],
+                          "algorithmic_bytes": nbytes, "frac_of_peak": round(nbytes / (us / 1e6) / 1e9 / peak, 4),
+                          "peak": f"{peak} GB/s {peak_kind}", "env_steps_per_s": E * T / (us / 1e6),
+                          "timing": "cold L2 (2 x L2 memset before each call), one call between two events, "
+                                    "min over 5 trials of the median of 50"}), flush=True)
+        del d, o
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_ncu_case(args):
     """Four calls of one estimator on one seeded batch and nothing else: the
     command line ncu captures (``--ncu-case vt,4096,128,em`` -> launches 0..3,
@@ -914,6 +967,8 @@ def main():
     ap.add_argument("--torch-baseline", action="store_true",
                     help="time the vectorised PyTorch doubling-scan baseline beside this library")
     ap.add_argument("--skip-torch-compile", action="store_true", help="with --torch-baseline: eager only")
+    ap.add_argument("--pages-protocol", action="store_true",
+                    help="time the named configurations with the paper's protocol (cold L2, isolated calls)")
     ap.add_argument("--ncu-case", default="",
                     help="KIND,E,T,em|tm[,bf16]: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()
@@ -925,6 +980,8 @@ def main():
         return run_sweep(args)
     if args.torch_baseline:
         return run_torch_baseline(args)
+    if args.pages_protocol:
+        return run_pages_protocol(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
