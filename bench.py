@@ -899,6 +899,7 @@ def run_pages_protocol(args):
     for kind, E, T, trunc in PAGES_PROTOCOL_CASES:
         d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
         o = [torch.empty(sh, dtype=dt, device=dev) for sh, dt in spec]
+        torch.cuda.synchronize()  # the inputs were written on the default stream
         with torch.cuda.stream(stream):
             for _ in range(20):
                 _sweep_call(kind, d, o, False)
