@@ -7,16 +7,21 @@ gamma = 0.99, lambda = 0.95 (the "thousands of environments, short
 rollouts" regime of rl-triton, arXiv:2608.17641, §6-§7).
 
 One step = GAE, discounted returns and TD(lambda) of one batch, computed by
-one fused launch (rlca_value_targets); the three separate entry points are
-timed as well.  The metric is env-steps per second per estimator:
-3 * E * T * steps / time.  Inputs stay resident in HBM; the timed steps
-rotate over enough replicas of the batch that their footprint exceeds
-three times the L2 cache, so every step reads from DRAM.
+one fused launch (rlca_value_targets) that writes advantages, returns
+(which are the TD(lambda) returns, bit for bit) and discounted returns; the
+three separate entry points are timed as well.  The metric is env-steps per
+second per estimator: E * T * steps / time (each step evaluates all three
+estimators over the same E * T env-steps).  Inputs stay resident in HBM;
+the timed steps rotate over enough replicas of the batch that their
+footprint exceeds three times the L2 cache, so every step reads from DRAM.
+The K timed launches are one CUDA graph whose first and last nodes are the
+two timing events, so the time is the device's from the first launch to
+the last, whatever K is.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
-oracle on the same workload instead.
+oracle (the C reference, over all host cores) on the same workload instead.
 """
 from __future__ import annotations
 
@@ -44,6 +49,8 @@ N_EST = 3
 METRIC = "env-steps/s per estimator at 4096 envs x 128 steps"
 WORKLOAD = "gae+discounted_return+td_lambda f32 4096x128 env-major"
 FALLBACK_HBM_GBS = 6800.0
+# longest timed region captured as a single graph bracketed by its own events
+MAX_GRAPH_STEPS = 50000
 
 
 def _workload_config(extra=None):
@@ -85,16 +92,35 @@ def _max_over_ranks(x, device):
 
 
 def _job_value(world, ms, steps):
-    """Whole-job throughput: every rank processed its own E x T shard per
-    step for every estimator, in the slowest rank's time."""
-    return world * N_EST * E * T * steps / (ms / 1e3)
+    """Whole-job throughput per estimator: every rank processed its own
+    E x T shard per step (for each of the N_EST estimators), in the slowest
+    rank's time."""
+    return world * E * T * steps / (ms / 1e3)
 
 
 # --------------------------------------------------------------------------
 # CPU oracle (the reported baseline and the reference arm)
 # --------------------------------------------------------------------------
 
+def _oracle_inputs(d, rows):
+    """The first ``rows`` environments of a batch as float64 / uint8 NumPy
+    arrays (converted once, outside any timing)."""
+    import numpy as np
+    from first_order_linear_gb300 import synth
+    n = synth.numpy(d)
+    out = {}
+    for k, v in n.items():
+        if isinstance(v, np.ndarray):
+            v = v[:rows]
+            v = np.ascontiguousarray(v.astype(np.uint8) if v.dtype == np.bool_ or v.dtype == np.uint8
+                                     else v.astype(np.float64))
+        out[k] = v
+    return out
+
+
 def _oracle_step(ref, n):
+    """GAE, discounted return and TD(lambda) of one batch with one oracle
+    module (the NumPy one or the C one: same signatures)."""
     ref.gae(n["rewards"], n["values"], n["terminated"], n["truncated"], n["trunc_value"], n["bootstrap"],
             gamma=GAMMA, lam=LAMBDA)
     ref.discounted_return(n["rewards"], n["terminated"], n["truncated"], n["trunc_value"], n["bootstrap"],
@@ -103,26 +129,87 @@ def _oracle_step(ref, n):
                   gamma=GAMMA, lam=LAMBDA)
 
 
-def _oracle_rows(d, rows):
-    from first_order_linear_gb300 import synth
-    n = synth.numpy(d)
-    return {k: (v[:rows] if isinstance(v, type(n["rewards"])) else v) for k, v in n.items()}
+def _row_slices(n, parts):
+    """``n`` split into ``parts`` contiguous row ranges (the oracle's rows
+    are independent)."""
+    rows = n["rewards"].shape[0]
+    cuts = [rows * i // parts for i in range(parts + 1)]
+    out = []
+    for lo, hi in zip(cuts[:-1], cuts[1:]):
+        if hi > lo:
+            out.append({k: (v[lo:hi] if getattr(v, "ndim", 0) >= 1 else v) for k, v in n.items()})
+    return out
 
 
-def cpu_baseline(d, budget_s=8.0):
-    """The oracle as it stands, on the host, over repeated full batches."""
-    from oracle import rlca_ref as ref
-    n = _oracle_rows(d, E)
+class OracleRunner:
+    """The C oracle (oracle/rlca_ref.c, float64 loops over one row at a
+    time) run over a batch by ``threads`` host threads, each on its own
+    contiguous block of environments.  ctypes releases the interpreter lock
+    during the C loops, so the threads run in parallel."""
+
+    def __init__(self, threads):
+        import concurrent.futures as cf
+        from oracle import ref_c
+        ref_c.load()
+        self.ref = ref_c
+        self.threads = threads
+        self.pool = cf.ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+
+    def step(self, n):
+        if self.pool is None:
+            _oracle_step(self.ref, n)
+            return
+        for f in [self.pool.submit(_oracle_step, self.ref, part) for part in _row_slices(n, self.threads)]:
+            f.result()
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _time_oracle(step, n, budget_s):
+    """Repeats ``step(n)`` for about ``budget_s`` seconds; (repeats, seconds)."""
+    step(n)  # first call: library load, page faults
     reps, t0 = 0, time.perf_counter()
     while True:
-        _oracle_step(ref, n)
+        step(n)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 1000:
-            break
-    return {"value": N_EST * E * T * reps / el, "unit": "env-steps/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} full {E}x{T} batches (GAE, discounted return, TD(lambda)) in float64 NumPy, "
-                      f"{el:.1f} s on one host thread"}
+        if el >= budget_s or reps >= 2000:
+            return reps, el
+
+
+def cpu_baseline(d, budget_s=6.0):
+    """The oracle as it stands, on the host: the C reference over all host
+    cores (the reported value), and single-threaded figures of the C and
+    the NumPy references beside it."""
+    from oracle import rlca_ref
+    n = _oracle_inputs(d, E)
+    cores = _host_cores()
+    runner = OracleRunner(cores)
+    try:
+        reps, el = _time_oracle(runner.step, n, budget_s)
+    finally:
+        runner.close()
+    one = OracleRunner(1)
+    reps1, el1 = _time_oracle(one.step, n, budget_s / 2)
+    nrows = max(64, E // 8)
+    sub = _oracle_inputs(d, nrows)
+    repsn, eln = _time_oracle(lambda x: _oracle_step(rlca_ref, x), sub, budget_s / 2)
+    return {"value": E * T * reps / el, "unit": "env-steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full {E}x{T} batches (GAE, discounted return, TD(lambda) each) through the C "
+                      f"float64 oracle, rows split over {cores} host threads, {el:.1f} s",
+            "c_oracle_1_thread": {"value": E * T * reps1 / el1, "cores": 1,
+                                  "sample": f"{reps1} full batches, {el1:.1f} s"},
+            "numpy_oracle_1_thread": {"value": nrows * T * repsn / eln, "cores": 1,
+                                      "sample": f"{repsn} batches of the first {nrows} envs, {eln:.1f} s"}}
 
 
 def run_reference(args):
@@ -130,29 +217,31 @@ def run_reference(args):
     if rank != 0:
         return 0
     d = _batch_cpu()
-    from oracle import rlca_ref as ref
-    n = _oracle_rows(d, E)
+    cores = _host_cores()
+    runner = OracleRunner(cores)
+    n = _oracle_inputs(d, E)
     t0 = time.perf_counter()
-    _oracle_step(ref, n)
+    runner.step(n)
     t_full = time.perf_counter() - t0
     # bound the whole run to about a minute of CPU work
     rows = E if (args.steps + args.warmup) * t_full <= 60.0 else max(
-        32, int(E * 60.0 / ((args.steps + args.warmup) * t_full)))
-    sub = _oracle_rows(d, rows)
+        cores, int(E * 60.0 / ((args.steps + args.warmup) * t_full)))
+    sub = _oracle_inputs(d, rows)
     for _ in range(args.warmup):
-        _oracle_step(ref, sub)
+        runner.step(sub)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(ref, sub)
+        runner.step(sub)
     el = time.perf_counter() - t0
-    units = N_EST * rows * T * args.steps
-    value = units / el
-    sample = f"first {rows} of {E} envs x {T} steps per step, GAE + discounted return + TD(lambda), float64 NumPy"
+    runner.close()
+    value = rows * T * args.steps / el
+    sample = (f"first {rows} of {E} envs x {T} steps per step, GAE + discounted return + TD(lambda), C float64 "
+              f"oracle, rows split over {cores} host threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "env-steps/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _workload_config({"rows_per_step": rows}),
-            "cpu_baseline": {"value": value, "unit": "env-steps/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "env-steps/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "env-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -248,13 +337,18 @@ def _recorded_traffic():
 
 def _calls(lib, P):
     """The C-ABI calls of one step's estimators on a replica x and stream s."""
-    def fused(x, s, flags=0x10):  # RLCA_INPUTS_READY: each step's inputs are resident before the timed region
+    def fused(x, s, flags=0x10, td=None):  # RLCA_INPUTS_READY: each step's inputs are resident before the timed region
+        # the returns written to ret are the TD(lambda) returns, bit for bit:
+        # the step writes them once (td=None), not a second identical copy
         return lib.rlca_value_targets(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
                                       P(x["trunc_value"]), P(x["bootstrap"]), P(x["adv"]), P(x["ret"]), P(x["disc"]),
-                                      P(x["td"]), E, T, GAMMA, LAMBDA, flags, None, 0, s)
+                                      P(td), E, T, GAMMA, LAMBDA, flags, None, 0, s)
 
     def fused_serial(x, s):
         return fused(x, s, flags=0)
+
+    def fused_td_copy(x, s):
+        return fused(x, s, td=x["td"])
 
     def gae(x, s):
         return lib.rlca_gae(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
@@ -270,7 +364,7 @@ def _calls(lib, P):
         return lib.rlca_td_lambda(P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
                                   P(x["trunc_value"]), P(x["bootstrap"]), P(x["td"]), E, T, GAMMA, LAMBDA, 0, None,
                                   0, s)
-    return fused, fused_serial, gae, disc, td
+    return fused, fused_serial, fused_td_copy, gae, disc, td
 
 
 def _capture(reps, fns, stream):
@@ -285,6 +379,50 @@ def _capture(reps, fns, stream):
                 if st != 0:
                     raise RuntimeError(f"capture failed with status {st}")
     return g
+
+
+def _timed_graph(reps, fn, stream, steps, first=0):
+    """One CUDA graph of ``steps`` launches of ``fn`` on consecutive replicas
+    (starting at replica ``first``), with a timing event recorded as the
+    graph's first node and another as its last: the events time the device
+    from the first launch to the end of the last, without the host's graph
+    submission.  Returns (graph, start event, end event), or None when this
+    PyTorch cannot record events inside a capture."""
+    import torch
+    try:
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        s = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        a.record()
+        for i in range(steps):
+            st = fn(reps[(first + i) % len(reps)], s)
+            if st != 0:
+                raise RuntimeError(f"capture failed with status {st}")
+        b.record()
+    return g, a, b
+
+
+def _upload(g, stream):
+    """cudaGraphUpload of a captured graph on ``stream``: a graph's first
+    replay otherwise uploads its launch work node by node as it runs
+    (measured here at 0.3-0.5 us per launch node), a one-time cost of the
+    graph, not of the steps it holds.  Returns True when the upload ran."""
+    import torch
+    try:
+        handle = g.raw_cuda_graph_exec()
+        rt = C.CDLL("libcudart.so.13")
+        rt.cudaGraphUpload.argtypes = [C.c_void_p, C.c_void_p]
+        rt.cudaGraphUpload.restype = C.c_int
+        ok = rt.cudaGraphUpload(C.c_void_p(handle), C.c_void_p(stream.cuda_stream)) == 0
+    except (AttributeError, OSError, RuntimeError, TypeError):
+        return False
+    stream.synchronize()
+    torch.cuda.synchronize()
+    return ok
 
 
 def _graph_us(g, launches, stream, replays=20):
@@ -350,7 +488,7 @@ def run_ours(args):
     footprint = nb * (in_bytes + out_bytes)
 
     P = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
-    fused, fused_serial, gae, disc, td = _calls(lib, P)
+    fused, fused_serial, fused_td_copy, gae, disc, td = _calls(lib, P)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):  # first calls (device attribute cache) outside capture
         for x in reps:
@@ -360,32 +498,58 @@ def run_ours(args):
     stream.synchronize()
 
     # the timed region: one fused launch per step, consecutive steps on
-    # consecutive replicas, captured as graphs of a full rotation (plus the
-    # remainder) and replayed back to back
-    full = _capture(reps, [fused], stream)
-    rem_n = args.steps % nb
-    rem = _capture(reps[:rem_n], [fused], stream) if rem_n else None
+    # consecutive replicas.  The warm-up steps are a graph of their own; the
+    # K timed steps are one graph bracketed by its own timing events (for K
+    # up to MAX_GRAPH_STEPS), so a short run measures the same steady state
+    # as a long one.  Beyond that: graphs of one rotation, replayed back to
+    # back, every one of them replayed once before the timed region.
+    warm = _capture([reps[i % nb] for i in range(args.warmup)], [fused], stream)
+    timed = _timed_graph(reps, fused, stream, args.steps, first=args.warmup) \
+        if args.steps <= MAX_GRAPH_STEPS else None
+    full = rem = None
+    uploaded = False
+    if timed is not None:
+        uploaded = _upload(timed[0], stream)
+    if timed is None:
+        full = _capture(reps, [fused], stream)
+        rem_n = args.steps % nb
+        rem = _capture(reps[:rem_n], [fused], stream) if rem_n else None
+        with torch.cuda.stream(stream):
+            full.replay()
+            if rem is not None:
+                rem.replay()
+        stream.synchronize()
 
     sampler = ClockSampler(dev.index, args.clock_log or None)
     sampler.start()
     with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(args.warmup / nb))):
-            full.replay()
+        warm.replay()
     stream.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        t_start.record()
-        for _ in range(args.steps // nb):
-            full.replay()
-        if rem is not None:
-            rem.replay()
-        t_end.record()
+    if timed is not None:
+        g_timed, t_start, t_end = timed
+        with torch.cuda.stream(stream):
+            g_timed.replay()
+        timing_how = ("one CUDA graph of the K launches whose first and last nodes are the two CUDA events "
+                      "(device time from the first launch to the end of the last)"
+                      + ("; the graph uploaded (cudaGraphUpload) before the timed region" if uploaded else
+                         "; graph not uploaded beforehand (its first replay uploads it)"))
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t_start.record()
+            for _ in range(args.steps // nb):
+                full.replay()
+            if rem is not None:
+                rem.replay()
+            t_end.record()
+        timing_how = ("CUDA events on the launching stream around back-to-back replays of graphs of one "
+                      "rotation (each replayed once before)")
     stream.synchronize()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -396,17 +560,18 @@ def run_ours(args):
     ms = _max_over_ranks(ms, dev)
     ms_per_step = ms / args.steps
     value = _job_value(world, ms, args.steps)
+    del warm, full, rem, timed
 
     # per-kernel figures, each from a graph of one rotation of that launch
     kern = {}
     for name, fns in (("value_targets_fused", [fused]), ("value_targets_fused_without_inputs_ready", [fused_serial]),
+                      ("value_targets_fused_with_separate_td_copy", [fused_td_copy]),
                       ("gae", [gae]), ("discounted_return", [disc]), ("td_lambda", [td]),
                       ("unfused_step_gae_disc_td", [gae, disc, td])):
         g = _capture(reps, fns, stream)
         us = _graph_us(g, nb, stream)
         kern[name] = {"us_per_launch" if len(fns) == 1 else "us_per_step": us,
-                      "env_steps_per_s_per_estimator": (N_EST if len(fns) != 1 or name.startswith("value") else 1)
-                      * E * T / (us / 1e6)}
+                      "env_steps_per_s_per_estimator": E * T / (us / 1e6)}
         del g
     # the public Python call (rlca.rlca_value_targets), launches in plain
     # stream order without graphs: host wall time per call
@@ -419,7 +584,10 @@ def run_ours(args):
     kern["value_targets_full_call"] = {"us_per_call": _full_call_us(api_call, reps, stream),
                                        "timing": "host wall clock over 200 back-to-back public-API calls"}
     n_trunc = int(d_cpu["truncated"].sum())
-    fused_bytes = E * T * (4 + 4 + 1 + 1 + 4 * 4) + 32 * n_trunc + 4 * E
+    # read r, V (4 B), two flag bytes; write adv, ret (= TD(lambda)), disc
+    # (4 B); the truncation values at one 32-byte sector per truncated step;
+    # the bootstrap vector
+    fused_bytes = E * T * (4 + 4 + 1 + 1 + 3 * 4) + 32 * n_trunc + 4 * E
     peak, peak_kind = _peaks()
     # context, not the path: a plain torch device copy moving the same bytes
     # per launch (half read, half written), captured and replayed the same
@@ -445,16 +613,18 @@ def run_ours(args):
     roofline = {"bound": "hbm", "kernel": "em_fast_kernel<ValueTargetsEst<true>,32,4> (rlca_value_targets)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "traffic": _recorded_traffic(),
-                "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_us": avg_us,
-                "timing": "timed region / steps: CUDA events on the launching stream around the K back-to-back "
-                          "launches (one launch per step; consecutive launches overlap)"}
+                "algorithmic_bytes_per_launch": fused_bytes,
+                "algorithmic_bytes_note": "22 B per env-step (r, V, 2 flags in; adv, ret = TD(lambda), disc out) "
+                                          "+ 32 B per truncated step + 4 B per env; a separate TD(lambda) copy "
+                                          "(bit-identical to ret) is not written and not counted",
+                "avg_launch_us": avg_us, "timing": "timed region / steps: " + timing_how}
 
     e2e = None if args.skip_e2e else run_e2e(args, d_cpu, dev)
     if e2e is not None and world > 1:
         # whole job: every rank's shard through its own host link, in the
         # slowest rank's time
         e2e_ms = _max_over_ranks(e2e["ms_per_step"], dev)
-        e2e.update(ms_per_step=e2e_ms, value=world * N_EST * E * T / (e2e_ms / 1e3),
+        e2e.update(ms_per_step=e2e_ms, value=world * E * T / (e2e_ms / 1e3),
                    h2d_bytes_per_step=world * e2e["h2d_bytes_per_step"],
                    d2h_bytes_per_step=world * e2e["d2h_bytes_per_step"], ranks=world)
     cpu = None
@@ -469,7 +639,8 @@ def run_ours(args):
                       f"{l2 / 2**20:.0f} MiB); no flush",
                 "launch": "one fused rlca_value_targets launch per step with RLCA_INPUTS_READY (inputs resident "
                           "before the timed region, so consecutive steps overlap through programmatic dependent "
-                          "launch); CUDA graphs of one rotation of consecutive steps, replayed back to back"}),
+                          "launch), writing advantages, returns (= TD(lambda) returns) and discounted returns; "
+                          + timing_how}),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps, "kernels": kern, "wall_s_timed_region": wall}
     if rank == 0:
@@ -482,12 +653,13 @@ def run_ours(args):
 def run_e2e(args, d_cpu, dev):
     """Same metric through the public Python API with host buffers: every
     step copies its inputs from pinned host memory to the device, runs the
-    fused value-target call and copies its four outputs back.  Steps are
+    fused value-target call and copies its three outputs back.  Steps are
     pipelined as a data loader would: the copy in on one stream, the call on
     a second, the copy out on a third, over two device buffer sets, so step
     k's inputs arrive while step k-1 computes and step k-2's outputs leave.
     A step's inputs sit packed in one pinned block and its outputs in one
-    [4, E, T] block: one copy each way."""
+    [3, E, T] block: one copy each way.  The same copies without the call,
+    in the same pipeline, give the host link's ceiling for this step."""
     import torch
     from first_order_linear_gb300 import rlca
 
@@ -508,8 +680,8 @@ def run_e2e(args, d_cpu, dev):
     NB = 2
     dev_blocks = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(NB)]
     devb = [views(blk) for blk in dev_blocks]
-    outs = [torch.empty(4, E, T, device=dev) for _ in range(NB)]
-    back = [torch.empty(4, E, T, pin_memory=True) for _ in range(NB)]
+    outs = [torch.empty(3, E, T, device=dev) for _ in range(NB)]
+    back = [torch.empty(3, E, T, pin_memory=True) for _ in range(NB)]
     h2d = sum(d_cpu[k].numel() * d_cpu[k].element_size() for k in names)
     d2h = back[0].numel() * back[0].element_size()
     steps = max(10, min(args.steps, 2000))
@@ -517,46 +689,56 @@ def run_e2e(args, d_cpu, dev):
     ev_in = [torch.cuda.Event() for _ in range(NB)]
     ev_run = [torch.cuda.Event() for _ in range(NB)]
     ev_out = [torch.cuda.Event() for _ in range(NB)]
-    started = [False] * NB
 
-    def step(i):
-        j = i % NB
-        x, o = devb[j], outs[j]
-        with torch.cuda.stream(s_in):
-            if started[j]:
-                s_in.wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
-            dev_blocks[j].copy_(host_block, non_blocking=True)
-            ev_in[j].record(s_in)
-        with torch.cuda.stream(s_run):
-            s_run.wait_event(ev_in[j])
-            if started[j]:
-                s_run.wait_event(ev_out[j])  # its previous outputs have left
-            rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"],
-                                    x["trunc_value"], x["bootstrap"], gamma=GAMMA, lambda_=LAMBDA,
-                                    advantages=o[0], returns=o[1], disc_returns=o[2], td_lambda_returns=o[3],
-                                    stream=s_run)
-            ev_run[j].record(s_run)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_run[j])
-            back[j].copy_(o, non_blocking=True)
-            ev_out[j].record(s_out)
-        started[j] = True
+    def pipeline(n, call):
+        started = [False] * NB
 
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
-    for i in range(steps):
-        step(i)
-    b.record(s_out)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b)
-    return {"value": N_EST * E * T * steps / (ms / 1e3), "unit": "env-steps/s", "h2d_bytes_per_step": h2d,
+        def step(i):
+            j = i % NB
+            x, o = devb[j], outs[j]
+            with torch.cuda.stream(s_in):
+                if started[j]:
+                    s_in.wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
+                dev_blocks[j].copy_(host_block, non_blocking=True)
+                ev_in[j].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(ev_in[j])
+                if started[j]:
+                    s_run.wait_event(ev_out[j])  # its previous outputs have left
+                if call:
+                    rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"],
+                                            x["trunc_value"], x["bootstrap"], gamma=GAMMA, lambda_=LAMBDA,
+                                            advantages=o[0], returns=o[1], disc_returns=o[2],
+                                            outputs=("advantages", "returns", "disc_returns"), stream=s_run)
+                ev_run[j].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[j])
+                back[j].copy_(o, non_blocking=True)
+                ev_out[j].record(s_out)
+            started[j] = True
+
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        for i in range(n):
+            step(i)
+        b.record(s_out)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
+    ms = pipeline(steps, True)
+    ms_link = pipeline(steps, False)
+    return {"value": E * T * steps / (ms / 1e3), "unit": "env-steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "host_link_ceiling": {"value": E * T * steps / (ms_link / 1e3), "ms_per_step": ms_link / steps,
+                                  "GBps_in_plus_out": (h2d + d2h) * steps / (ms_link / 1e3) / 1e9,
+                                  "how": "the same pipelined pinned copies in and out, without the call"},
+            "frac_of_host_link_ceiling": ms_link / ms,
             "pipeline": "one packed copy in, the call, one packed copy out per step, on three streams over "
-                        "two device buffer sets (bound by the host link: 15.7 MB per step)"}
+                        "two device buffer sets"}
 
 
 # --------------------------------------------------------------------------
@@ -583,7 +765,7 @@ def _sweep_case(kind, E, T, trunc, dev, bf16=False):
     if kind in ("gae", "disc", "td", "vt"):
         d = synth.value_rollout(E, T, seed, p_term=P_TERM, p_trunc=P_TRUNC, with_trunc=trunc, device=dev)
         reads = {"gae": 2, "disc": 1, "td": 2, "vt": 2}[kind] * fe + 1
-        outs = {"gae": 2, "disc": 1, "td": 1, "vt": 4}[kind]
+        outs = {"gae": 2, "disc": 1, "td": 1, "vt": 3}[kind]  # vt: adv, ret (= TD(lambda)), disc
         spec = [((E, T), fdt)] * outs
     elif kind == "vtrace":
         d = synth.vtrace_rollout(E, T, seed, p_term=0.01, p_trunc=P_TRUNC if trunc else 0.0, with_trunc=trunc,
@@ -618,7 +800,8 @@ def _sweep_call(kind, x, o, tm, ready=False):
         rlca.rlca_td_lambda(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, out=o[0], **kw)
     elif kind == "vt":
         rlca.rlca_value_targets(x["rewards"], x["values"], *b, gamma=GAMMA, lambda_=LAMBDA, advantages=o[0],
-                                returns=o[1], disc_returns=o[2], td_lambda_returns=o[3], **kw)
+                                returns=o[1], disc_returns=o[2], outputs=("advantages", "returns", "disc_returns"),
+                                **kw)
     elif kind == "vtrace":
         rlca.rlca_vtrace(x["rewards"], x["values"], x["logp_target"], x["logp_behaviour"], *b, gamma=GAMMA, vs=o[0],
                          pg_advantages=o[1], **kw)
@@ -928,32 +1111,52 @@ def run_pages_protocol(args):
 
 
 def run_ncu_case(args):
-    """Four calls of one estimator on one seeded batch and nothing else: the
-    command line ncu captures (``--ncu-case vt,4096,128,em`` -> launches 0..3,
-    capture with ``-s 2 -c 1``)."""
+    """Calls of one estimator and nothing else: the command lines ncu
+    captures.  ``--ncu-case vt,4096,128,em`` makes four calls on one seeded
+    batch (capture with ``-s 2 -c 1``).  With the option ``rot``
+    (``vt,4096,128,em,rot``) the calls rotate over replicas whose footprint
+    exceeds 3 x L2, 4 rotations in plain stream order, as the bench's timed
+    region does; a capture with ``--cache-control none`` of a launch in the
+    third rotation then sees the DRAM traffic of the steady state (reads of
+    inputs no longer in L2, write-backs of outputs evicted from it).
+    Option ``bf16``: bfloat16 storage."""
     import torch
     from first_order_linear_gb300 import build, synth
     parts = args.ncu_case.split(",")
     kind, E, T, lay = parts[:4]
-    bf16 = len(parts) > 4 and parts[4] == "bf16"
+    opts = set(parts[4:])
+    bf16, rot = "bf16" in opts, "rot" in opts
     E, T, tm = int(E), int(T), lay == "tm"
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     d, nbytes, spec = _sweep_case(kind, E, T, True, dev, bf16=bf16)
     x = {k: (synth.to_time_major(v) if tm and isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    o = [torch.empty(sh if not tm else (sh[1], sh[0]), dtype=dt, device=dev) for sh, dt in spec]
-    for _ in range(4):
-        _sweep_call(kind, x, o, tm)
+    nb = 1
+    if rot:
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+        foot = sum(v.numel() * v.element_size() for v in x.values() if isinstance(v, torch.Tensor))
+        foot += sum(E * T * torch.empty(0, dtype=dt).element_size() for _, dt in spec)
+        nb = max(2, math.ceil(3 * l2 / foot))
+    reps = []
+    for i in range(nb):
+        xi = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in x.items()} if rot else x
+        reps.append((xi, [torch.empty(sh if not tm else (sh[1], sh[0]), dtype=dt, device=dev) for sh, dt in spec]))
+    calls = 4 * nb if rot else 4
     torch.cuda.synchronize()
-    print(json.dumps({"ncu_case": args.ncu_case, "algorithmic_bytes_per_call": nbytes}))
+    for i in range(calls):
+        xi, o = reps[i % nb]
+        _sweep_call(kind, xi, o, tm)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": args.ncu_case, "algorithmic_bytes_per_call": nbytes, "calls": calls,
+                      "replicas": nb}))
     return 0
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu-baseline", action="store_true")

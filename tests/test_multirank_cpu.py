@@ -47,7 +47,7 @@ def test_two_gloo_ranks_shard_and_agree_on_time(tmp_path):
     # every rank sees the slowest rank's time
     assert float(r[0]["ms"]) == pytest.approx(2.5) and float(r[1]["ms"]) == pytest.approx(2.5)
     # whole-job value: both shards' env-steps for every estimator, in that time
-    want = world * bench.N_EST * bench.E * bench.T * 10 / 2.5e-3
+    want = world * bench.E * bench.T * 10 / 2.5e-3  # env-steps per second per estimator
     assert float(r[0]["value"]) == pytest.approx(want) and float(r[1]["value"]) == pytest.approx(want)
     # the shards are the same shape but different environments
     assert r[0]["rewards"].shape == r[1]["rewards"].shape == (bench.E, bench.T)
@@ -58,4 +58,4 @@ def test_two_gloo_ranks_shard_and_agree_on_time(tmp_path):
 def test_single_process_needs_no_group():
     import bench
     assert bench._max_over_ranks(3.25, torch.device("cpu")) == 3.25
-    assert bench._job_value(1, 2.0, 4) == pytest.approx(bench.N_EST * bench.E * bench.T * 4 / 2e-3)
+    assert bench._job_value(1, 2.0, 4) == pytest.approx(bench.E * bench.T * 4 / 2e-3)
