@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     """Compile (if sources changed) and return the path of librlca.so."""
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
-    stamp = LIB + ".stamp"
+    stamp = os.path.join(BUILD, "librlca.so.stamp")  # build-cache fingerprint, not product source
     fp = _fingerprint()
     if not force and not ptxas_info and os.path.exists(LIB) and os.path.exists(stamp):
         with open(stamp) as f:

@@ -6,10 +6,13 @@
 // up front).  For them the scratch lives in one file-scope device array of
 // RLCA_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
 // exit.  Host code only sees a stand-in for that array's name, so its device
-// address is looked up once per device (with that device current) and handed
-// to the kernel like any workspace.  Nothing here allocates.
+// address is looked up once per device context (with that device current)
+// and handed to the kernel like any workspace.  Nothing here allocates.
+#include <cuda.h>  // CUcontext / CUresult types of the two driver calls below
+
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "rlca.h"
@@ -20,17 +23,74 @@ constexpr int kMaxDevices = 256;
 
 static __device__ __align__(256) unsigned char g_gae_scratch[RLCA_STATIC_SCRATCH_BYTES];
 
-std::atomic<void*> g_scratch_addr[kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 
-// set-up: device address of g_gae_scratch on the current device
+// The array's address belongs to the device context the module was loaded
+// into: after cudaDeviceReset (or any teardown of the primary context) the
+// module is loaded again and the array may sit elsewhere.  Each cached
+// address is therefore stored with the unique id of its context and looked
+// up again when the current context's id differs.  The driver's
+// cuCtxGetCurrent and cuCtxGetId are reached through the runtime's entry
+// point query, so the library still links only the runtime.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+struct CtxApi {
+  CtxGetCurrentFn current = nullptr;
+  CtxGetIdFn id = nullptr;
+};
+
+const CtxApi& ctx_api() {
+  static const CtxApi api = [] {
+    CtxApi a;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.id = reinterpret_cast<CtxGetIdFn>(f);
+    return a;
+  }();
+  return api;
+}
+
+// unique id of the context current on this thread; 0 when there is none or
+// it cannot be told (then the address is looked up on every call)
+unsigned long long current_context_id() {
+  const CtxApi& a = ctx_api();
+  if (a.current == nullptr || a.id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (a.current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return a.id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+struct ScratchSlot {
+  std::mutex m;
+  unsigned long long ctx = 0;  // context the address was looked up in
+  void* addr = nullptr;
+};
+ScratchSlot g_slot[kMaxDevices];
+
+// set-up: device address of g_gae_scratch on the current device, looked up
+// on a device's first call and again whenever its context has changed
 cudaError_t scratch_address(int dev, void** out) {
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    cudaError_t e = cudaGetSymbolAddress(&p, g_gae_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+  ScratchSlot& s = g_slot[dev];
+  std::lock_guard<std::mutex> lock(s.m);
+  const unsigned long long id = current_context_id();
+  if (s.addr != nullptr && id != 0 && id == s.ctx) {
+    *out = s.addr;
+    return cudaSuccess;
   }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_gae_scratch);  // makes the device's context current
+  if (e != cudaSuccess) return e;
+  s.addr = p;
+  s.ctx = current_context_id();
   *out = p;
   return cudaSuccess;
 }
@@ -95,6 +155,7 @@ extern "C" int rlca_gae_static_scratch(const float* rewards, const float* values
   g.vec = (!p.time_major && vec && T % 4 == 0) ? 1 : 0;
   g.early = 0;
   g.ws = ws;
+  g.aux = nullptr;
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
   cudaError_t e;
   if (truncated) {

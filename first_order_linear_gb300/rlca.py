@@ -134,6 +134,20 @@ def _stream(device, stream):
     return s.cuda_stream
 
 
+def _hold(device, stream, *tensors):
+    """Marks device tensors the call reads or writes as in use on ``stream``
+    when that is not the current stream.  Buffers this module allocates
+    (the workspace, outputs not passed in) come from the caching allocator
+    on the current stream; without the mark, memory freed there could be
+    handed to new work on the current stream while the kernel on ``stream``
+    still reads or writes it."""
+    if stream is None or stream == torch.cuda.current_stream(device):
+        return
+    for t in tensors:
+        if t is not None:
+            t.record_stream(stream)
+
+
 def _boundaries(shape, dev, terminated, truncated, trunc_value, bootstrap, E, F=_F):
     _check(terminated, "terminated", _U8, shape, dev, required=False)
     _check(truncated, "truncated", _U8, shape, dev, required=False)
@@ -169,6 +183,7 @@ def rlca_gae(rewards, values, terminated=None, truncated=None, trunc_value=None,
         check("rlca_gae", lib.rlca_gae(
             _ptr(rewards), _ptr(values), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap),
             _ptr(advantages), _ptr(returns), E, T, gamma, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
+        _hold(dev, stream, ws, advantages, returns)
     return advantages, returns
 
 
@@ -204,6 +219,7 @@ def rlca_value_targets(rewards, values, terminated=None, truncated=None, trunc_v
             _ptr(rewards), _ptr(values), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap),
             _ptr(bufs["advantages"]), _ptr(bufs["returns"]), _ptr(bufs["disc_returns"]),
             _ptr(bufs["td_lambda_returns"]), E, T, gamma, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
+        _hold(dev, stream, ws, *bufs.values())
     return bufs["advantages"], bufs["returns"], bufs["disc_returns"], bufs["td_lambda_returns"]
 
 
@@ -229,6 +245,7 @@ def rlca_discounted_return(rewards, terminated=None, truncated=None, trunc_value
         check("rlca_discounted_return", lib.rlca_discounted_return(
             _ptr(rewards), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap), _ptr(out),
             E, T, gamma, flags, _ptr(ws), wsb, _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out
 
 
@@ -255,6 +272,7 @@ def rlca_td_lambda(rewards, values, terminated=None, truncated=None, trunc_value
         check("rlca_td_lambda", lib.rlca_td_lambda(
             _ptr(rewards), _ptr(values), _ptr(terminated), _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap),
             _ptr(out), E, T, gamma, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out
 
 
@@ -287,6 +305,7 @@ def rlca_vtrace(rewards, values, logp_target, logp_behaviour, terminated=None, t
             _ptr(rewards), _ptr(values), _ptr(logp_target), _ptr(logp_behaviour), _ptr(terminated),
             _ptr(truncated), _ptr(trunc_value), _ptr(bootstrap), _ptr(vs), _ptr(pg_advantages), E, T,
             gamma, rho_bar, c_bar, lambda_, flags, _ptr(ws), wsb, _stream(dev, stream)))
+        _hold(dev, stream, ws, vs, pg_advantages)
     return vs, pg_advantages
 
 
@@ -320,6 +339,7 @@ def rlca_retrace(q, pi, mu_a, actions, rewards, terminated=None, truncated=None,
             _ptr(q), _ptr(pi), _ptr(mu_a), _ptr(actions), _ptr(rewards), _ptr(terminated), _ptr(truncated),
             _ptr(trunc_value), _ptr(bootstrap), _ptr(out), E, T, A, gamma, lambda_, flags, _ptr(ws), wsb,
             _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out
 
 
@@ -345,6 +365,7 @@ def rlca_elig_trace(x, terminated=None, truncated=None, *, gamma=0.99, lambda_=0
         check("rlca_elig_trace", lib.rlca_elig_trace(
             _ptr(x), _ptr(terminated), _ptr(truncated), _ptr(out), E, T, gamma, lambda_, flags, _ptr(ws), wsb,
             _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out
 
 
@@ -376,6 +397,7 @@ def rlca_episodic_prefix_sum(x, terminated=None, truncated=None, *, exclusive=Fa
         check("rlca_episodic_prefix_sum", lib.rlca_episodic_prefix_sum(
             _ptr(x), dtype, _ptr(terminated), _ptr(truncated), _ptr(out), E, T, flags, _ptr(ws), wsb,
             _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out
 
 
@@ -401,4 +423,5 @@ def rlca_affine_scan(alpha, beta, carry=None, *, reverse=True, out=None, time_ma
         check("rlca_affine_scan", lib.rlca_affine_scan(
             _ptr(alpha), _ptr(beta), _ptr(carry), _ptr(out), E, T, 1 if reverse else 0, flags, _ptr(ws), wsb,
             _stream(dev, stream)))
+        _hold(dev, stream, ws, out)
     return out

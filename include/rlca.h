@@ -217,6 +217,10 @@ int rlca_value_targets(const float *rewards, const float *values,
  *
  *  - The first call on a device looks up that array's device address (the
  *    set-up); make that first call before any stream capture on the device.
+ *    The address is kept with the id of the device context it was found in
+ *    and looked up again when that context has changed (after
+ *    cudaDeviceReset, for instance): the first call after such a change is
+ *    a set-up call too.
  *  - Problems whose two-pass path needs more than RLCA_STATIC_SCRATCH_BYTES
  *    (8 bytes per row per segment; rlca_workspace_size with RLCA_EST_GAE
  *    gives the figure) return RLCA_ERR_UNSUPPORTED and enqueue nothing;

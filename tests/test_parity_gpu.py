@@ -470,3 +470,54 @@ def test_bf16_retrace_action_counts(A, tm):
     parity.check_case("retrace", 40, 200, seed=A, time_major=tm, bf16=True, num_actions=A)
     parity.check_case("retrace", 40, 200, seed=A + 1, time_major=tm, bf16=True, num_actions=A, shift=True)
 
+
+
+def test_side_stream_two_pass_workspace_survives_reuse():
+    """A call on a stream other than the current one, whose workspace and
+    outputs the binding allocates: memory the current stream allocates
+    right after the call must not alias them while the kernel runs."""
+    E, T = 64, 4096  # few environments, long rows: the two-pass path with a workspace
+    d = parity.make_inputs("gae", E, T, seed=11, trunc=True, device="cuda")
+    need = rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, E, T, 0, _lib.RLCA_MULTIPASS)
+    assert need > 0
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    rounds = []
+    for _ in range(4):
+        adv, ret = rlca.rlca_gae(d["rewards"], d["values"], d["terminated"], d["truncated"], d["trunc_value"],
+                                 d["bootstrap"], gamma=parity.GAMMA, lambda_=parity.LAMBDA, multipass=True,
+                                 stream=side)
+        # the current stream grabs and scribbles on fresh memory at once
+        junk = [torch.full((need // 4 + 1024,), float("nan"), device="cuda") for _ in range(4)]
+        del junk
+        rounds.append((adv, ret))
+    torch.cuda.synchronize()
+    want = parity.run_oracle("gae", d, np.arange(E))
+    for adv, ret in rounds:
+        parity.assert_close(adv.cpu().numpy(), want[0], "adv on a side stream")
+        parity.assert_close(ret.cpu().numpy(), want[1], "ret on a side stream")
+
+
+def test_retrace_two_pass_keeps_per_step_scalars():
+    """Retrace on the two-pass path: the workspace holds the segment maps and
+    three float planes of per-step (E_pi Q, Q(a), c), 12 bytes a step, which
+    the second pass reads instead of Q and pi; results match the oracle in
+    both layouts, also when the workspace held other data before."""
+    E, T = 1024, 2048
+    for tm in (True, False):
+        flags = _lib.RLCA_TIME_MAJOR if tm else 0
+        need = rlca.rlca_workspace_size(_lib.RLCA_EST_RETRACE, E, T, synth.NUM_ACTIONS, flags)
+        if need == 0:
+            continue  # this device runs the layout in one pass
+        assert need >= 12 * E * T
+        d = synth.retrace_rollout(E, T, seed=synth.config_seed("retrace-aux"), p_term=0.002, p_trunc=0.005,
+                                  with_trunc=True, device="cuda")
+        x = parity._tm(d, tm)
+        ws = torch.full((need,), 0x7F, dtype=torch.uint8, device="cuda")  # garbage the first pass must overwrite
+        out = rlca.rlca_retrace(x["q"], x["pi"], x["mu_a"], x["actions"], x["rewards"], x["terminated"],
+                                x["truncated"], x["trunc_value"], x["bootstrap"], gamma=parity.GAMMA,
+                                lambda_=parity.LAMBDA, time_major=tm, workspace=ws)
+        torch.cuda.synchronize()
+        rows = parity.sample_rows(E, T, seed=5, n=128)
+        want = parity.run_oracle("retrace", d, rows)
+        parity.assert_close(parity._np(parity._back(out, tm), rows), want[0], f"retrace two-pass tm={tm}")

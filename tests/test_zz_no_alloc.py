@@ -70,6 +70,29 @@ def test_static_scratch_matches_workspace_path(cuda_lib, E, T, tm, mp):
         _compare(ret, ref_ret, f"returns, call {call + 1}")
 
 
+@pytest.mark.parametrize("tm", [False, True], ids=["env_major", "time_major"])
+def test_static_scratch_single_pass_needs_no_scratch(cuda_lib, tm):
+    """4096 x 128 takes the one-pass drivers: the entry point must work
+    without ever looking at its scratch."""
+    E, T = 4096, 128
+    flags = _lib.RLCA_TIME_MAJOR if tm else 0
+    assert rlca.rlca_workspace_size(_lib.RLCA_EST_GAE, E, T, flags=flags) == 0
+    for call, seed in enumerate((303, 404)):
+        d = parity.make_inputs("gae", E, T, seed=seed, trunc=True, device="cuda")
+        x = parity._tm(d, tm)
+        shape = tuple(x["rewards"].shape)
+        adv = torch.full(shape, float("nan"), device="cuda")
+        ret = torch.full(shape, float("nan"), device="cuda")
+        status = _static_call(cuda_lib, x, tm, False, adv, ret)
+        assert status == _lib.RLCA_OK, cuda_lib.rlca_status_string(status)
+        ref_adv, ref_ret = rlca.rlca_gae(x["rewards"], x["values"], x["terminated"], x["truncated"],
+                                         x["trunc_value"], x["bootstrap"], gamma=parity.GAMMA,
+                                         lambda_=parity.LAMBDA, time_major=tm)
+        torch.cuda.synchronize()
+        _compare(adv, ref_adv, f"advantages, call {call + 1}")
+        _compare(ret, ref_ret, f"returns, call {call + 1}")
+
+
 def test_static_scratch_refuses_oversized_problems(cuda_lib):
     # time-major, forced two pass: 2100 rows x 64 segments x 8 B > 1 MiB
     E, T = 2100, 8192
