@@ -118,6 +118,8 @@ int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flag
   g.vec = (!p.time_major && vec_ok && T % 4 == 0) ? 1 : 0;
   g.early = (flags & RLCA_INPUTS_READY) ? 1 : 0;
   g.ws = ws;
+  g.aux = p.aux_bytes > 0 ? reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + aux_offset(p.ws_bytes, p.aux_bytes))
+                          : nullptr;
   return run_scan(est, p, g, s) == cudaSuccess ? RLCA_OK : RLCA_ERR_CUDA;
 }
 
@@ -188,6 +190,15 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   // one affine map per (row, segment): two values, two of each for the fused value targets
   const size_t ws_elem = kind == Kind::ValueTargets ? 16 : 8;
   q.ws_bytes = q.nseg > 1 ? (size_t)E * q.nseg * ws_elem : 0;
+  // Retrace's two passes: the first also leaves every step's (E_pi Q, Q(a),
+  // c) in three float planes after the maps (256-byte aligned), so the
+  // second reads 12 bytes a step instead of the 2 A values of Q and pi
+  q.aux_bytes = 0;
+  if (retrace && q.nseg > 1) {
+    q.ws_bytes = (q.ws_bytes + 255) & ~size_t(255);
+    q.aux_bytes = (size_t)3 * (size_t)E * (size_t)T * sizeof(float);
+    q.ws_bytes += q.aux_bytes;
+  }
   const bool fast_ok = !q.time_major && vec && q.nseg == 1 && !(flags & RLCA_MULTIPASS);
   q.fast = fast_ok && T % kEmSteps == 0 && q.ntiles == 1;
   q.steps = kEmSteps;

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
   const bool agg_mode = g.mode == kModeAggregate;
   const EnvMajor lay{g.E, g.T};
   const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (!early) pdl_wait();
 
   Aff<V> carry;
@@ -58,11 +59,10 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
     const int t0 = ts + j * L;
     const int n = row_ok ? max(0, min(L, te - t0)) : 0;
 
-    est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, ts, te, est_smem);
+    est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, g, row0, rloc, ts, te, est_smem);
     typename Est::template Regs<L> R;
     const GIO<EnvMajor, false, typename Est::Store> io{lay, row, t0, n, vec};
     est.template load<L>(R, io, rloc, ts, S::TILE, S::ROWS, est_smem);
-    if (it == ntiles - 1) pdl_trigger();
 
     if constexpr (Est::kNb > 0) {
       // neighbour step's inputs: from the adjacent lane when it holds them,
@@ -271,8 +271,44 @@ __device__ __forceinline__ void em_fast_scan(const Est& est, typename Est::templ
 // A thread therefore holds either all LS steps or none, and a thread
 // beyond its row's end contributes the identity map to the scan.
 // ---------------------------------------------------------------------------
+// Resident CTAs the fast env-major driver is compiled for.  One launch of a
+// short-row workload (4096 x 128: 1024 CTAs of 128 threads) fills about half
+// of the GPU's thread slots; consecutive launches overlap (the dependent
+// grid launches as soon as this one has started, see pdl_trigger) only as
+// far as the slots the running grid leaves free.  At 4 steps a thread the
+// estimators fit 32 registers (at most a few bytes spilled), which makes
+// every thread slot usable: 16 CTAs of 128 threads per SM.  Retrace (its
+// action-axis staging), V-Trace with truncation and the 8-step variants
+// spill tens to hundreds of bytes at 32 and keep the compiler's choice;
+// V-Trace without truncation fits with 20 bytes spilled but measured slower
+// capped in plain stream order (4096 x 256: 0.60 against 0.66 of the
+// bandwidth) and is left uncapped unless RLCA_EM_CAP_VTRACE is set.
+#ifndef RLCA_EM_CAP_VTRACE
+#define RLCA_EM_CAP_VTRACE 0
+#endif
+template <class Est>
+struct EmRegCap {
+  static constexpr bool value = true;
+};
+template <bool H, class ST>
+struct EmRegCap<RetraceEst<H, ST>> {
+  static constexpr bool value = false;
+};
+template <class ST>
+struct EmRegCap<VtraceEst<true, ST>> {
+  static constexpr bool value = false;
+};
+template <class ST>
+struct EmRegCap<VtraceEst<false, ST>> {
+  static constexpr bool value = RLCA_EM_CAP_VTRACE != 0;
+};
+template <class Est, int BLOCK, int LS>
+__host__ __device__ constexpr int em_fast_min_blocks() {
+  return (EmRegCap<Est>::value && LS == 4) ? 2048 / BLOCK : 1;
+}
+
 template <class Est, int TPR, int LS>
-__global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
+__global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK, (em_fast_min_blocks<Est, EmShape<TPR, LS>::BLOCK, LS>()))
     em_fast_kernel(Est est, Geom g) {
   using S = EmShape<TPR, LS>;
   using V = typename Est::V;
@@ -292,13 +328,13 @@ __global__ void __launch_bounds__(EmShape<TPR, LS>::BLOCK)
   const int n = active ? L : 0;
   const EnvMajor lay{g.E, g.T};
   const bool early = g.early != 0;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (!early) pdl_wait();
 
-  est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, row0, rloc, 0, g.T, est_smem);
+  est.template stage<S::ROWS, S::BLOCK, S::TILE>(lay, g, row0, rloc, 0, g.T, est_smem);
   typename Est::template Regs<L> R;
   const GIO<EnvMajor, true, typename Est::Store> io{lay, row, t0, n, true};
   est.template load<L>(R, io, rloc, 0, S::TILE, S::ROWS, est_smem);
-  pdl_trigger();
 
   em_fast_scan<Est, TPR, LS>(est, R, g, lay, row, t0, active, rloc, xw);
   if (early) pdl_wait();  // the previous kernel may still read or write what we overwrite
@@ -331,6 +367,7 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
   const bool agg_mode = g.mode == kModeAggregate;
   const TimeMajor lay{g.E, g.T};
   const bool early = g.early != 0 && g.nseg == 1 && !agg_mode;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (!early) pdl_wait();
 
   Aff<V> carry;
@@ -350,11 +387,10 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
     const int t0 = ts + cw * L;
     const int n = row_ok ? max(0, min(L, te - t0)) : 0;
 
-    est.template stage_tm<S::BLOCK>(lay, row0, ts, te, est_smem);
+    est.template stage_tm<S::BLOCK>(lay, g, row0, ts, te, est_smem);
     typename Est::template Regs<L> R;
     const GIO<TimeMajor, false, typename Est::Store> io{lay, row, t0, n, false};
     est.template load<L>(R, io, lane, ts, S::TILE, 32, est_smem);
-    if (it == ntiles - 1) pdl_trigger();
     if constexpr (Est::kNb > 0) {
       float got[Est::kNb > 0 ? Est::kNb : 1];
 #pragma unroll
@@ -471,6 +507,7 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
   const uint32_t E32 = (uint32_t)g.E;
   const TimeMajor lay{g.E, g.T};
   const bool early = g.early != 0 && g.nseg == 1;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (!early) pdl_wait();
 
   // scan role: the value entering this segment (full pass) or the map of
@@ -491,7 +528,6 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
-    if (it == ntiles - 1) pdl_trigger();
     if constexpr (Est::kNb > 0) {
       float got[Est::kNb > 0 ? Est::kNb : 1];
 #pragma unroll
@@ -610,6 +646,7 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
   const uint32_t e0 = (uint32_t)row0;
   const TimeMajor lay{g.E, g.T};
   const bool early = g.early != 0 && g.nseg == 1;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (!early) pdl_wait();
 
   StagedList in;
@@ -688,7 +725,6 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     stage_tile(it + NS - 1);  // into the stage every thread finished reading in iteration it - 1
     float nb_nxt[NB];
     nb_fetch(it + 1, nb_nxt);
-    if (it == ntiles - 1) pdl_trigger();
     const int tile = BWD ? ntiles - 1 - it : it;
     const int ts = seg_lo + tile * S::TILE;
     const int t0 = ts + c * L;
@@ -763,5 +799,7 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
   if (agg_mode && cs == 0 && row0 + js < g.E)
     reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
+
+
 
 }  // namespace rlca

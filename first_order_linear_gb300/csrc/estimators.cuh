@@ -37,9 +37,9 @@ namespace rlca {
 // Default no-op staging.
 struct NoStage {
   template <int ROWS, int BLOCK, int TILE, class Lay>
-  __device__ __forceinline__ void stage(const Lay&, int64_t, int, int, int, unsigned char*) const {}
+  __device__ __forceinline__ void stage(const Lay&, const Geom&, int64_t, int, int, int, unsigned char*) const {}
   template <int BLOCK, class Lay>
-  __device__ __forceinline__ void stage_tm(const Lay&, int64_t, int, int, unsigned char*) const {}
+  __device__ __forceinline__ void stage_tm(const Lay&, const Geom&, int64_t, int, int, unsigned char*) const {}
 };
 
 // Common boundary inputs of the backward estimators.
@@ -74,7 +74,7 @@ __device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryReg
 }
 
 template <class F>
-__device__ __forceinline__ void staged_flags(const BoundaryArgs& b, F& f) {
+__host__ __device__ __forceinline__ void staged_flags(const BoundaryArgs& b, F& f) {
   f.in_b(b.term);
   f.in_b(b.trunc);
 }
@@ -108,7 +108,7 @@ struct GaeEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
@@ -175,7 +175,7 @@ struct DiscEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     staged_flags(b, f);
   }
@@ -233,7 +233,7 @@ struct TdLambdaEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
@@ -304,7 +304,7 @@ struct ValueTargetsEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 2, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     staged_flags(b, f);
@@ -384,7 +384,7 @@ struct VtraceEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 4, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(r);
     f.in_f(v);
     f.in_f(lpt);
@@ -651,9 +651,12 @@ struct RetraceEst {
   __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
 
   // shared memory: per warp the raw Q and pi blocks (retrace_raw_floats),
-  // then the staged per-step scalars [3][ROWS][tile + 1]
+  // then the staged per-step scalars [3][ROWS][tile + 1].  On the two-pass
+  // path (g.aux set) the first pass also copies each tile's own steps'
+  // scalars to the planes g.aux, and the second pass fills the staged
+  // scalars from there instead of reading Q and pi again.
   template <int ROWS, int BLOCK, int TILE, class Lay>
-  __device__ __forceinline__ void stage(const Lay& lay, int64_t row0, int, int ts, int te,
+  __device__ __forceinline__ void stage(const Lay& lay, const Geom& g, int64_t row0, int, int ts, int te,
                                         unsigned char* sm) const {
     constexpr int NW = BLOCK / 32;
     constexpr int SROW = TILE + 1;  // tile + 1 steps per row
@@ -664,6 +667,20 @@ struct RetraceEst {
     float* s_qa = s_ev + ROWS * SROW;
     float* s_c = s_qa + ROWS * SROW;
     const int nst = te - ts + (te < b.T ? 1 : 0);
+    const int64_t plane = lay.E * (int64_t)lay.T;
+    if (g.aux != nullptr && g.mode == kModeFull) {
+      for (int i = threadIdx.x; i < ROWS * nst; i += BLOCK) {
+        const int rr = i / nst, k = i - rr * nst;
+        if (row0 + rr < lay.E) {
+          const int64_t gi = lay.at(row0 + rr, ts + k);
+          s_ev[rr * SROW + k] = g.aux[gi];
+          s_qa[rr * SROW + k] = g.aux[plane + gi];
+          s_c[rr * SROW + k] = g.aux[2 * plane + gi];
+        }
+      }
+      __syncthreads();
+      return;
+    }
     const int per_row = (nst + 31) / 32;
     st.template walk<retrace_bufs(false)>(ROWS * per_row, warp, NW, lane, raw, s_ev, s_qa, s_c,
             [&](int ch, int64_t* e0, int* cnt, int* slot) {
@@ -676,11 +693,24 @@ struct RetraceEst {
               return true;
             });
     __syncthreads();
+    if (g.aux != nullptr) {  // first pass: steps ts .. te-1 are this tile's own
+      const int own = te - ts;
+      for (int i = threadIdx.x; i < ROWS * own; i += BLOCK) {
+        const int rr = i / own, k = i - rr * own;
+        if (row0 + rr < lay.E) {
+          const int64_t gi = lay.at(row0 + rr, ts + k);
+          g.aux[gi] = s_ev[rr * SROW + k];
+          g.aux[plane + gi] = s_qa[rr * SROW + k];
+          g.aux[2 * plane + gi] = s_c[rr * SROW + k];
+        }
+      }
+    }
   }
   // time-major: one chunk = one step of 32 consecutive environments;
-  // staged scalars [3][tile + 1][32]
+  // staged scalars [3][tile + 1][32]; the planes as in stage()
   template <int BLOCK, class Lay>
-  __device__ __forceinline__ void stage_tm(const Lay& lay, int64_t row0, int ts, int te, unsigned char* sm) const {
+  __device__ __forceinline__ void stage_tm(const Lay& lay, const Geom& g, int64_t row0, int ts, int te,
+                                           unsigned char* sm) const {
     constexpr int NW = BLOCK / 32;
     constexpr int SROWS = (BLOCK / 32) * 8 + 1;
     __syncthreads();
@@ -691,6 +721,20 @@ struct RetraceEst {
     float* s_c = s_qa + SROWS * 32;
     const int nst = te - ts + (te < b.T ? 1 : 0);
     const int cnt = (int)min((int64_t)32, lay.E - row0);
+    const int64_t plane = lay.E * (int64_t)lay.T;
+    if (g.aux != nullptr && g.mode == kModeFull) {
+      for (int i = threadIdx.x; i < nst * 32; i += BLOCK) {
+        const int k = i >> 5, l = i & 31;
+        if (l < cnt) {
+          const int64_t gi = lay.at(row0 + l, ts + k);
+          s_ev[i] = g.aux[gi];
+          s_qa[i] = g.aux[plane + gi];
+          s_c[i] = g.aux[2 * plane + gi];
+        }
+      }
+      __syncthreads();
+      return;
+    }
     st.template walk<retrace_bufs(true)>(nst, warp, NW, lane, raw, s_ev, s_qa, s_c, [&](int i, int64_t* e0, int* c, int* slot) {
       *e0 = lay.at(row0, ts + i);
       *c = cnt;
@@ -698,6 +742,17 @@ struct RetraceEst {
       return true;
     });
     __syncthreads();
+    if (g.aux != nullptr) {  // first pass: steps ts .. te-1 are this tile's own
+      for (int i = threadIdx.x; i < (te - ts) * 32; i += BLOCK) {
+        const int k = i >> 5, l = i & 31;
+        if (l < cnt) {
+          const int64_t gi = lay.at(row0 + l, ts + k);
+          g.aux[gi] = s_ev[i];
+          g.aux[plane + gi] = s_qa[i];
+          g.aux[2 * plane + gi] = s_c[i];
+        }
+      }
+    }
   }
 
   template <int L, class IO>
@@ -767,7 +822,7 @@ struct EligEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(x);
     f.in_b(term);
     f.in_b(trunc);
@@ -833,7 +888,7 @@ struct PrefixSumEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 1, kSB = 2;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(x);
     f.in_b(term);
     f.in_b(trunc);
@@ -907,7 +962,7 @@ struct AffineEst : NoStage {
   static constexpr bool kStageable = true;
   static constexpr int kSF = 2, kSB = 0;  // staged float inputs, flag inputs
   template <class F>
-  __device__ __forceinline__ void staged_io(F& f) const {
+  __host__ __device__ __forceinline__ void staged_io(F& f) const {
     f.in_f(alpha);
     f.in_f(beta);
   }

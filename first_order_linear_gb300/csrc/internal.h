@@ -38,8 +38,12 @@ struct Plan {
   int64_t row_blocks;
   size_t smem;      // estimator staging shared memory per CTA (the launcher adds the driver's exchange arrays)
   size_t smem_driver_bound;  // upper bound of the driver's part, for the size check
-  size_t ws_bytes;  // workspace of the two-pass path
+  size_t ws_bytes;  // workspace of the two-pass path (segment maps, then aux_bytes)
+  size_t aux_bytes; // Retrace's per-step scalar planes at the workspace's end (two-pass path)
 };
+
+// byte offset of the Retrace scalar planes inside a two-pass workspace
+constexpr size_t aux_offset(size_t ws_bytes, size_t aux_bytes) { return ws_bytes - aux_bytes; }
 
 // Fills *p for a problem; returns false when the sizes cannot be launched.
 // vec: the env-major arrays are 16-byte aligned (4-byte for flags) and

@@ -157,8 +157,8 @@ struct StagedList {
   const void* fin[kMaxF];
   const uint8_t* bin[kMaxB];
   int nf = 0, nb = 0;
-  __device__ __forceinline__ void in_f(const void* p) { fin[nf++] = p; }
-  __device__ __forceinline__ void in_b(const uint8_t* p) { bin[nb++] = p; }
+  __host__ __device__ __forceinline__ void in_f(const void* p) { fin[nf++] = p; }
+  __host__ __device__ __forceinline__ void in_b(const uint8_t* p) { bin[nb++] = p; }
 };
 
 }  // namespace rlca

@@ -288,9 +288,13 @@ __device__ __forceinline__ void store_ints(int32_t* __restrict__ p, const Lay& l
 // serialization attribute, so a kernel may be scheduled while the previous
 // kernel of the stream drains.  pdl_wait() blocks until that kernel has
 // completed and its writes are visible (no-op when launched without the
-// attribute); it comes before the first global access.  pdl_trigger() lets
-// the next kernel of the stream start launching once every CTA of this grid
-// has issued it (or exited).
+// attribute); it comes before the first global access that may conflict
+// with it.  pdl_trigger() lets the next kernel of the stream start
+// launching once every CTA of this grid has issued it (or exited).  It
+// carries no memory ordering -- the next kernel's own pdl_wait() still
+// waits for this grid's completion -- so every driver issues it first
+// thing: the next launch's CTAs then take free SM slots (and, with
+// RLCA_INPUTS_READY, load their inputs) while this grid still runs.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -311,6 +315,8 @@ struct Geom {
   int early;    // inputs do not depend on the previous kernel of the stream: load
                 // before waiting on it, wait only before the first global write
   void* ws;     // [E][nseg] affine maps of the segments (two-pass path)
+  float* aux;   // Retrace, two-pass path: per-step (E_pi Q, Q(a_t), c_t) as three
+                // planes of E * T floats in the call's element order (else null)
 };
 
 // consecutive steps per thread in the env-major driver (a multiple of 4:
