@@ -651,18 +651,22 @@ def run_ours(args):
 
 
 def run_e2e(args, d_cpu, dev):
-    """Same metric through the public Python API with host buffers: every
-    step copies its inputs from pinned host memory to the device, runs the
-    fused value-target call and copies its three outputs back.  Steps are
-    pipelined as a data loader would: the copy in on one stream, the call on
-    a second, the copy out on a third, over two device buffer sets, so step
-    k's inputs arrive while step k-1 computes and step k-2's outputs leave.
-    A step's inputs sit packed in one pinned block and its outputs in one
-    [3, E, T] block: one copy each way.  The same copies without the call,
-    in the same pipeline, give the host link's ceiling for this step."""
+    """Same metric end to end through the C ABI with host buffers: every step
+    copies its inputs from pinned host memory to the device, runs the fused
+    value-target call (rlca_value_targets) and copies its three outputs back
+    to pinned host memory.  Steps are pipelined as a data loader would: the
+    copy in on one stream, the call on a second, the copy out on a third,
+    over two device buffer sets, so step k's inputs arrive while step k-1
+    computes and step k-2's outputs leave.  A step's inputs sit packed in one
+    pinned block and its outputs in one [3, E, T] block: one copy each way.
+    The pipeline of STEPS_PER_GRAPH steps is captured once as a CUDA graph
+    (copies, calls and the streams' event dependencies) and replayed, so the
+    host issues one launch per STEPS_PER_GRAPH steps.  The same graph without
+    the calls gives the host link's ceiling for this step."""
     import torch
-    from first_order_linear_gb300 import rlca
+    from first_order_linear_gb300 import _lib
 
+    lib = _lib.load()
     names = [k for k, v in d_cpu.items() if v is not None]
     offs, size = {}, 0
     for k in names:  # every tensor starts on a 256-byte boundary
@@ -684,61 +688,87 @@ def run_e2e(args, d_cpu, dev):
     back = [torch.empty(3, E, T, pin_memory=True) for _ in range(NB)]
     h2d = sum(d_cpu[k].numel() * d_cpu[k].element_size() for k in names)
     d2h = back[0].numel() * back[0].element_size()
-    steps = max(10, min(args.steps, 2000))
+    STEPS_PER_GRAPH = 20
+    P = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    s_main = torch.cuda.Stream(dev)
     s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(NB)]
-    ev_run = [torch.cuda.Event() for _ in range(NB)]
-    ev_out = [torch.cuda.Event() for _ in range(NB)]
 
-    def pipeline(n, call):
+    def capture(call):
+        """One graph of STEPS_PER_GRAPH pipelined steps (fork from the
+        capture stream onto the three pipeline streams, join at the end)."""
+        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_run = [torch.cuda.Event() for _ in range(NB)]
+        ev_out = [torch.cuda.Event() for _ in range(NB)]
         started = [False] * NB
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_main):
+            for st in (s_in, s_run, s_out):
+                st.wait_stream(s_main)
+            for i in range(STEPS_PER_GRAPH):
+                j = i % NB
+                x, o = devb[j], outs[j]
+                with torch.cuda.stream(s_in):
+                    if started[j]:
+                        s_in.wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
+                    dev_blocks[j].copy_(host_block, non_blocking=True)
+                    ev_in[j].record(s_in)
+                with torch.cuda.stream(s_run):
+                    s_run.wait_event(ev_in[j])
+                    if started[j]:
+                        s_run.wait_event(ev_out[j])  # its previous outputs have left
+                    if call:
+                        st = lib.rlca_value_targets(
+                            P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
+                            P(x["trunc_value"]), P(x["bootstrap"]), P(o[0]), P(o[1]), P(o[2]), None, E, T, GAMMA,
+                            LAMBDA, 0, None, 0, C.c_void_p(s_run.cuda_stream))
+                        if st != 0:
+                            raise RuntimeError(f"rlca_value_targets failed with status {st}")
+                    ev_run[j].record(s_run)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_run[j])
+                    back[j].copy_(o, non_blocking=True)
+                    ev_out[j].record(s_out)
+                started[j] = True
+            for st in (s_in, s_run, s_out):
+                s_main.wait_stream(st)
+        _upload(g, s_main)
+        return g
 
-        def step(i):
-            j = i % NB
-            x, o = devb[j], outs[j]
-            with torch.cuda.stream(s_in):
-                if started[j]:
-                    s_in.wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
-                dev_blocks[j].copy_(host_block, non_blocking=True)
-                ev_in[j].record(s_in)
-            with torch.cuda.stream(s_run):
-                s_run.wait_event(ev_in[j])
-                if started[j]:
-                    s_run.wait_event(ev_out[j])  # its previous outputs have left
-                if call:
-                    rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"],
-                                            x["trunc_value"], x["bootstrap"], gamma=GAMMA, lambda_=LAMBDA,
-                                            advantages=o[0], returns=o[1], disc_returns=o[2],
-                                            outputs=("advantages", "returns", "disc_returns"), stream=s_run)
-                ev_run[j].record(s_run)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_run[j])
-                back[j].copy_(o, non_blocking=True)
-                ev_out[j].record(s_out)
-            started[j] = True
-
-        for i in range(3):
-            step(i)
+    def timed(g, reps):
+        with torch.cuda.stream(s_main):
+            g.replay()  # warm-up replay
         torch.cuda.synchronize(dev)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(s_in)
-        for i in range(n):
-            step(i)
-        b.record(s_out)
+        with torch.cuda.stream(s_main):
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
         torch.cuda.synchronize(dev)
-        return a.elapsed_time(b)
+        return a.elapsed_time(b), reps * STEPS_PER_GRAPH
 
-    ms = pipeline(steps, True)
-    ms_link = pipeline(steps, False)
+    reps = max(1, min(args.steps, 2000) // STEPS_PER_GRAPH)
+    g_call = capture(True)
+    ms, steps = timed(g_call, reps)
+    del g_call
+    g_link = capture(False)
+    ms_link, _ = timed(g_link, reps)
+    del g_link
+    # the results of the last step reached the host: check them against the
+    # device outputs (the copies are part of the step, not a formality)
+    torch.cuda.synchronize(dev)
+    last = (steps - 1) % NB
+    if not torch.equal(back[last], outs[last].cpu()):
+        raise RuntimeError("e2e: host copy of the outputs differs from the device outputs")
     return {"value": E * T * steps / (ms / 1e3), "unit": "env-steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
             "host_link_ceiling": {"value": E * T * steps / (ms_link / 1e3), "ms_per_step": ms_link / steps,
                                   "GBps_in_plus_out": (h2d + d2h) * steps / (ms_link / 1e3) / 1e9,
                                   "how": "the same pipelined pinned copies in and out, without the call"},
             "frac_of_host_link_ceiling": ms_link / ms,
-            "pipeline": "one packed copy in, the call, one packed copy out per step, on three streams over "
-                        "two device buffer sets"}
+            "pipeline": f"per step one packed pinned-host copy in, the C-ABI call, one packed copy out, on three "
+                        f"streams over two device buffer sets; {STEPS_PER_GRAPH} steps per CUDA graph, replayed"}
 
 
 # --------------------------------------------------------------------------

@@ -10,7 +10,11 @@ import ctypes as C
 import os
 import threading
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librlca.so")
+# RLCA_LIBRARY=checked selects the index-check build of the same sources
+# (librlca_checked.so: every call waits for its kernels and fails when one of
+# them met an index outside its array); the default is the product build
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                         "librlca_checked.so" if os.environ.get("RLCA_LIBRARY") == "checked" else "librlca.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -40,6 +44,8 @@ RLCA_F32 = 0
 RLCA_I32 = 1
 RLCA_MAX_ACTIONS = 64
 RLCA_STATIC_SCRATCH_BYTES = 1 << 20
+RLCA_STATUS_WAIT_TIMEOUT = 0x1
+RLCA_STATUS_INDEX = 0x2
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -52,6 +58,8 @@ _sz = C.c_size_t
 SIGNATURES = {
     "rlca_status_string": (C.c_char_p, [_i]),
     "rlca_version": (_i, []),
+    "rlca_device_status": (_i, [C.POINTER(C.c_uint), _i]),
+    "rlca_index_checks": (_i, []),
     "rlca_workspace_size": (_i, [_i, _i64, _i64, C.c_int32, _u32, C.POINTER(_sz)]),
     "rlca_gae": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p, _sz, _p]),
     "rlca_value_targets": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _i64, _f, _f, _u32, _p, _sz, _p]),

@@ -101,13 +101,45 @@ int with_storage(uint32_t flags, F&& f) {
 // bytes of one float-array element
 size_t fbytes(uint32_t flags) { return (flags & RLCA_BF16) ? 2 : 4; }
 
+}  // namespace
+
+// Index-check build (RLCA_INDEX_CHECK): every call waits for its kernels and
+// fails with RLCA_ERR_CUDA when one of them recorded a condition in a device
+// status word (the bits stay readable through rlca_device_status).  The
+// product build returns RLCA_OK without waiting.
+int checked_build_status(cudaStream_t s) {
+  if constexpr (!kIndexCheck) {
+    (void)s;
+    return RLCA_OK;
+  } else {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RLCA_ERR_CUDA;
+    unsigned int w = 0;
+    if (rlca_device_status(&w, 0) != RLCA_OK) return RLCA_ERR_CUDA;
+    return w == 0 ? RLCA_OK : RLCA_ERR_CUDA;
+  }
+}
+
+namespace {
+
 template <class Est>
 int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flags, void* ws, size_t ws_bytes,
            bool vec_ok, cudaStream_t s) {
   int sm = 0;
   if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
+  // tensor-copy staging of time-major tiles: every staged input on a
+  // 16-byte boundary (the copies' rule), E % 16 == 0 (16-byte flag rows)
+  bool bulk = false;
+  if constexpr (Est::kStageable) {
+    if ((flags & RLCA_TIME_MAJOR) && E % 16 == 0 && tensor_maps_available()) {
+      StagedList in;
+      est.staged_io(in);
+      bulk = true;
+      for (int i = 0; i < in.nf; ++i) bulk = bulk && aligned(in.fin[i], 16);
+      for (int i = 0; i < in.nb; ++i) bulk = bulk && aligned(in.bin[i], 16);
+    }
+  }
   Plan p;
-  if (!make_plan(kind, E, (int)T, A, flags, sm, vec_ok && T % 4 == 0, &p)) return RLCA_ERR_INVALID_ARG;
+  if (!make_plan(kind, E, (int)T, A, flags, sm, vec_ok && T % 4 == 0, &p, bulk)) return RLCA_ERR_INVALID_ARG;
   if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes || !aligned(ws, 16))) return RLCA_ERR_INVALID_ARG;
   Geom g;
   g.E = E;
@@ -120,13 +152,14 @@ int launch(Kind kind, const Est& est, int64_t E, int64_t T, int A, uint32_t flag
   g.ws = ws;
   g.aux = p.aux_bytes > 0 ? reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + aux_offset(p.ws_bytes, p.aux_bytes))
                           : nullptr;
-  return run_scan(est, p, g, s) == cudaSuccess ? RLCA_OK : RLCA_ERR_CUDA;
+  if (run_scan(est, p, g, s) != cudaSuccess) return RLCA_ERR_CUDA;
+  return checked_build_status(s);
 }
 
 }  // namespace
 
 bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec,
-               Plan* out) {
+               Plan* out, bool bulk) {
   const bool retrace = kind == Kind::Retrace;
   Plan q = {};
   q.time_major = (flags & RLCA_TIME_MAJOR) != 0;
@@ -248,9 +281,25 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     // (with two or more float inputs the direct 8-environment driver measured faster)
     const bool one_float = kind == Kind::Disc || kind == Kind::Elig || kind == Kind::PrefixSum;
     const bool staged16 = kTmStaged16 && one_float && vec && !bf16_io && E % 4 == 0 && tf_ew == 8;
-    const bool staged = staged32 || staged16;
-    const int EW = staged16 ? 16 : tf_ew;
-    const int CT = staged32 ? std::min(tf_ct, 8) : tf_ct;
+    bool staged = staged32 || staged16;
+    int EW = staged16 ? 16 : tf_ew;
+    int CT = staged32 ? std::min(tf_ct, 8) : tf_ct;
+    // bulk: each tile of each input is one tensor copy into a ring of
+    // RLCA_TB_STAGES stages, 32 environments per CTA, once E gives two such
+    // CTAs per SM; chunk-threads so the ring stays within kTbRingBytes and a
+    // CTA within 256 threads.  (With fewer environments, 16-environment
+    // CTAs -- the narrowest whose flag rows are 16 bytes -- measured slower
+    // than the direct 8-environment driver, split into two passes or not.)
+    const StageCounts sc = stage_counts(kind);
+    const size_t step_bytes = (size_t)sc.nf * (bf16_io ? 2 : 4) + (size_t)sc.nb;
+    if (kTmBulk && bulk && E % 16 == 0 && E >= (int64_t)kTbMinEnvsPerSm * sm_count) {
+      EW = 32;
+      const int ct_min = 32 / EW;  // whole warps
+      CT = std::max(ct_min, std::min(ct_need, 256 / EW));
+      while (CT > ct_min && (size_t)RLCA_TB_STAGES * 8 * CT * EW * step_bytes > kTbRingBytes) CT /= 2;
+      staged = false;
+      q.tm_bulk = true;
+    }
     q.tm_fast = true;
     q.tm_staged = staged;
     q.env_width = EW;
@@ -266,7 +315,16 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     const int64_t threads = q.row_blocks * q.block;
     const int64_t target = (int64_t)sm_count * 1024;
     int ns = 1;
-    if (q.ntiles > 4 && 2 * threads < target) ns = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
+    if (q.tm_bulk) {
+      // the bulk driver keeps its tiles in flight by copies, not threads:
+      // split rows across CTAs until there are kTbCtasPerSm CTAs an SM (a
+      // second pass re-reads the inputs, from L2 while they fit there)
+      const int64_t want = (int64_t)kTbCtasPerSm * sm_count;
+      if (q.ntiles > 1 && q.row_blocks < want)
+        ns = (int)std::min<int64_t>(q.ntiles, (want + q.row_blocks - 1) / q.row_blocks);
+    } else if (q.ntiles > 4 && 2 * threads < target) {
+      ns = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
+    }
     const int seg_tiles = (q.ntiles + ns - 1) / ns;
     q.seg_len = seg_tiles * q.tile;
     q.nseg = (q.ntiles + seg_tiles - 1) / seg_tiles;
@@ -275,11 +333,77 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     q.smem_driver_bound = (size_t)CT * (EW + 1) * (kMaxMapBytes + kMaxMapBytes / 2);
     // the stages: at most 4 float and 2 flag inputs of CT * (8 * EW + EW) elements
     if (staged) q.smem_driver_bound += (size_t)RLCA_TS_STAGES * ((size_t)CT * 9 * EW * 18 + 16);
+    // barriers, alignment slack and the tensor-copy ring
+    if (q.tm_bulk) q.smem_driver_bound += 256 + (size_t)RLCA_TB_STAGES * 8 * CT * EW * step_bytes;
   }
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
 
   *out = q;
+  return true;
+}
+
+StageCounts stage_counts(Kind kind) {
+  switch (kind) {
+    case Kind::Gae:
+    case Kind::TdLambda:
+    case Kind::ValueTargets: return {2, 2};
+    case Kind::Disc:
+    case Kind::Elig:
+    case Kind::PrefixSum: return {1, 2};
+    case Kind::Vtrace: return {4, 2};
+    case Kind::Affine: return {2, 0};
+    default: return {0, 0};
+  }
+}
+
+namespace {
+
+// the driver's tensor-map encoder, reached through the runtime's entry-point
+// query (the library links only the runtime)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// [T, E] array of elem_bytes elements, E innermost; boxes of ew x rows; the
+// copy moves bits, so the element type only gives the size
+bool encode_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t E, int64_t T, int ew, int rows) {
+  const EncodeTiledFn fn = encoder();
+  if (fn == nullptr) return false;
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT32;
+  const cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)E * (cuuint64_t)elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)ew, (cuuint32_t)rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tensor_maps_available() { return encoder() != nullptr; }
+
+bool encode_tm_maps(const StagedList& in, int elem_bytes, int64_t E, int64_t T, int ew, int rows, TmaSet* out) {
+  for (int i = 0; i < in.nf; ++i)
+    if (!encode_2d(&out->f[i], in.fin[i], elem_bytes, E, T, ew, rows)) return false;
+  for (int i = 0; i < in.nb; ++i)
+    if (in.bin[i] != nullptr && !encode_2d(&out->b[i], in.bin[i], 1, E, T, ew, rows)) return false;
   return true;
 }
 
@@ -299,7 +423,21 @@ const char* rlca_status_string(int status) {
   }
 }
 
-int rlca_version(void) { return 100; }
+int rlca_version(void) { return 200; }
+
+int rlca_index_checks(void) { return kIndexCheck ? 1 : 0; }
+
+int rlca_device_status(unsigned int* status, int clear) {
+  if (status == nullptr) return RLCA_ERR_INVALID_ARG;
+  *status = 0;
+  const bool c = clear != 0;
+  cudaError_t (*const units[])(unsigned int*, bool) = {status_values, status_values_bf16_a, status_values_bf16_b,
+                                                       status_offpolicy, status_offpolicy_bf16, status_forward,
+                                                       status_forward_bf16};
+  for (auto f : units)
+    if (f(status, c) != cudaSuccess) return RLCA_ERR_CUDA;
+  return RLCA_OK;
+}
 
 int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions, uint32_t flags, size_t* bytes) {
   if (bytes == nullptr) return RLCA_ERR_INVALID_ARG;
@@ -328,10 +466,11 @@ int rlca_workspace_size(int estimator, int64_t E, int64_t T, int32_t num_actions
   if (sm_count_of_current_device(&sm) != cudaSuccess) return RLCA_ERR_CUDA;
   // the call picks the staged or the direct path from its pointers' alignment,
   // which the query cannot see: report the larger of the two needs
-  Plan pd, ps;
+  Plan pd, ps, pb;
   if (!make_plan(kind, E, (int)T, num_actions, flags & kFloatFlags, sm, false, &pd)) return RLCA_ERR_INVALID_ARG;
   if (!make_plan(kind, E, (int)T, num_actions, flags & kFloatFlags, sm, true, &ps)) return RLCA_ERR_INVALID_ARG;
-  *bytes = std::max(pd.ws_bytes, ps.ws_bytes);
+  if (!make_plan(kind, E, (int)T, num_actions, flags & kFloatFlags, sm, true, &pb, true)) return RLCA_ERR_INVALID_ARG;
+  *bytes = std::max(std::max(pd.ws_bytes, ps.ws_bytes), pb.ws_bytes);
   return RLCA_OK;
 }
 
@@ -521,7 +660,7 @@ int rlca_retrace(const float* q, const float* pi, const float* mu_a, const int32
   const BoundaryArgs b{terminated, truncated, trunc_value, bootstrap, (int)T};
   return with_storage(flags, [&](auto tag) {
     using ST = typename decltype(tag)::type;
-    const RetraceStage<ST> stg{q, pi, mu_a, actions, num_actions, lambda};
+    const RetraceStage<ST> stg{q, pi, mu_a, actions, num_actions, lambda, E * T};
     if (truncated) {
       RetraceEst<true, ST> e;
       e.b = b; e.st = stg; e.r = rewards; e.out = q_ret; e.gamma = gamma;

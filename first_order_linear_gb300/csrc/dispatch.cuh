@@ -125,6 +125,55 @@ static cudaError_t launch_ts_any(const Plan& p, const Est& est, const Geom& g, c
   return cudaErrorInvalidConfiguration;
 }
 
+template <class Est, int EW, int CT>
+static cudaError_t launch_tb(const Plan& p, const Est& est, const Geom& g, cudaStream_t s, const TmaSet& maps) {
+  if constexpr (WidthCaps<Est>::tm_fast && Est::kStageable) {
+    void (*kernel)(Est, Geom, const TmaSet) = tm_bulk_kernel<Est, EW, CT>;
+    const size_t smem = tb_smem_bytes<Est, EW, CT>();
+    if (smem > kMaxSmemPerCta) return cudaErrorInvalidConfiguration;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.row_blocks * p.nseg));
+    cfg.blockDim = dim3((unsigned)p.block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, est, g, maps);
+  } else {
+    return cudaErrorInvalidConfiguration;
+  }
+}
+
+template <class Est>
+static cudaError_t launch_tb_any(const Plan& p, const Est& est, const Geom& g, cudaStream_t s, const TmaSet& maps) {
+  if (p.env_width == 16) {
+    switch (p.width) {
+      case 2: return launch_tb<Est, 16, 2>(p, est, g, s, maps);
+      case 4: return launch_tb<Est, 16, 4>(p, est, g, s, maps);
+      case 8: return launch_tb<Est, 16, 8>(p, est, g, s, maps);
+      case 16: return launch_tb<Est, 16, 16>(p, est, g, s, maps);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  if (p.env_width == 32) {
+    switch (p.width) {
+      case 1: return launch_tb<Est, 32, 1>(p, est, g, s, maps);
+      case 2: return launch_tb<Est, 32, 2>(p, est, g, s, maps);
+      case 4: return launch_tb<Est, 32, 4>(p, est, g, s, maps);
+      case 8: return launch_tb<Est, 32, 8>(p, est, g, s, maps);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
 template <class Est>
 static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
   if (p.env_width == 32) {
@@ -163,7 +212,7 @@ static cudaError_t launch_tf_any(const Plan& p, const Est& est, const Geom& g, c
 }
 
 template <class Est>
-static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cudaStream_t s) {
+static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cudaStream_t s, const TmaSet& maps) {
   if (p.fast) {
     switch (p.width) {
       case 1: return launch_fast_w<Est, 1>(p, est, g, s);
@@ -180,6 +229,7 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
       default: return cudaErrorInvalidConfiguration;
     }
   }
+  if (p.tm_bulk) return launch_tb_any(p, est, g, s, maps);
   if (p.tm_fast) return p.tm_staged ? launch_ts_any(p, est, g, s) : launch_tf_any(p, est, g, s);
   if (p.time_major) {
     switch (p.width) {
@@ -210,14 +260,38 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
 
 template <class Est>
 cudaError_t run_scan(const Est& est, const Plan& p, const Geom& g0, cudaStream_t s) {
+  TmaSet maps;  // filled for the bulk driver only (the other drivers never read it)
+  if constexpr (Est::kStageable) {
+    if (p.tm_bulk) {
+      maps = TmaSet{};
+      StagedList in;
+      est.staged_io(in);
+      if (!encode_tm_maps(in, (int)sizeof(typename Est::Store), g0.E, g0.T, p.env_width, p.tile, &maps))
+        return cudaErrorInvalidValue;
+    }
+  }
   Geom g = g0;
   if (p.nseg > 1) {
     g.mode = kModeAggregate;
-    cudaError_t e = launch_pass(p, est, g, s);
+    cudaError_t e = launch_pass(p, est, g, s, maps);
     if (e != cudaSuccess) return e;
   }
   g.mode = kModeFull;
-  return launch_pass(p, est, g, s);
+  return launch_pass(p, est, g, s, maps);
+}
+
+// The device status word of the kernels of the translation unit that
+// includes this header (tma.cuh): ORed into *word, zeroed with clear.
+static cudaError_t tu_status(unsigned int* word, bool clear) {
+  unsigned int w = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&w, g_tu_status, sizeof(w));
+  if (e != cudaSuccess) return e;
+  *word |= w;
+  if (clear && w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_tu_status, &zero, sizeof(zero));
+  }
+  return e;
 }
 
 }  // namespace rlca

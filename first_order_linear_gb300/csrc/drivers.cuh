@@ -5,6 +5,7 @@
 #pragma once
 
 #include "estimators.cuh"
+#include "tma.cuh"
 
 namespace rlca {
 
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
         got[i] = BWD ? __shfl_down_sync(kFullMask, give[i], 1, GW) : __shfl_up_sync(kFullMask, give[i], 1, GW);
       const int tn = BWD ? t0 + L : t0 - 1;
       const bool edge = BWD ? (lig == GW - 1 || t0 + L >= te) : (lig == 0);
-      if (n > 0 && edge && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (n > 0 && edge && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T))
+        est.nb_load(lay, row, tn, got);
       est.nb_take(R, got);
     }
 
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(EmShape<TPR>::BLOCK)
     }
     carry = next_carry;
   }
-  if (agg_mode && row_ok && j == 0) reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
+  if (agg_mode && row_ok && j == 0 && in_range(row * g.nseg + seg, g.E * (int64_t)g.nseg))
+    reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -189,7 +192,8 @@ __device__ __forceinline__ void em_fast_scan(const Est& est, typename Est::templ
     if constexpr (NWR > 1) {
       const int tn = BWD ? t0 + L : t0 - 1;
       const bool edge = BWD ? (lane == 31) : (lane == 0);
-      if (active && edge && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (active && edge && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T))
+        est.nb_load(lay, row, tn, got);
     }
     est.nb_take(R, got);
   }
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
 #pragma unroll
       for (int i = 0; i < Est::kNb; ++i) got[i] = 0.f;
       const int tn = BWD ? t0 + L : t0 - 1;
-      if (n > 0 && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (n > 0 && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T)) est.nb_load(lay, row, tn, got);
       est.nb_take(R, got);
     }
 
@@ -452,7 +456,8 @@ __global__ void __launch_bounds__(TmShape<C>::BLOCK)
     }
     carry = cc;
   }
-  if (agg_mode && row_ok && cw == 0) reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
+  if (agg_mode && row_ok && cw == 0 && in_range(row * g.nseg + seg, g.E * (int64_t)g.nseg))
+    reinterpret_cast<Aff<V>*>(g.ws)[row * g.nseg + seg] = carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -524,7 +529,8 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
     const int ts = seg_lo + tile * S::TILE;
     const int t0 = ts + c * L;
     const int n = (row_ok && t0 < seg_hi) ? L : 0;
-    const TmIO32<typename Est::Store> io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32};
+    const TmIO32<typename Est::Store> io{row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row, E32,
+                                               E32 * (uint32_t)g.T};
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
 #pragma unroll
       for (int i = 0; i < Est::kNb; ++i) got[i] = 0.f;
       const int tn = BWD ? t0 + L : t0 - 1;
-      if (n > 0 && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (n > 0 && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T)) est.nb_load(lay, row, tn, got);
       est.nb_take(R, got);
     }
 
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(TfShape<EW, CT>::BLOCK, tf_min_blocks(TfShape<
     if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
     est.template store<L>(R, io);
   }
-  if (agg_mode && cs == 0 && row0 + js < g.E)
+  if (agg_mode && cs == 0 && row0 + js < g.E && in_range((row0 + js) * g.nseg + seg, g.E * (int64_t)g.nseg))
     reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
 
@@ -670,9 +676,11 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
         if (t < g.T && e < E32) {
           const uint32_t go = (uint32_t)t * E32 + e;
           const int so = (r / L) * CS + (r % L) * EW + FPE * q;
+          if (span_in_range(go, FPE, (int64_t)E32 * g.T) && span_in_range(so, FPE, FB)) {
 #pragma unroll
-          for (int b = 0; b < Est::kSF; ++b)
-            cp_async16(reinterpret_cast<ST*>(st) + b * FB + so, static_cast<const ST*>(in.fin[b]) + go);
+            for (int b = 0; b < Est::kSF; ++b)
+              cp_async16(reinterpret_cast<ST*>(st) + b * FB + so, static_cast<const ST*>(in.fin[b]) + go);
+          }
         }
       }
       // flag inputs: 4-byte pieces of 4 environments
@@ -685,9 +693,11 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
         if (t < g.T && e < E32) {
           const uint32_t go = (uint32_t)t * E32 + e;
           const int so = (r / L) * CS + (r % L) * EW + 4 * q;
+          if (span_in_range(go, 4, (int64_t)E32 * g.T) && span_in_range(so, 4, FB)) {
 #pragma unroll
-          for (int b = 0; b < Est::kSB; ++b)
-            if (in.bin[b] != nullptr) cp_async4(st + FLAGS_AT + b * FB + so, in.bin[b] + go);
+            for (int b = 0; b < Est::kSB; ++b)
+              if (in.bin[b] != nullptr) cp_async4(st + FLAGS_AT + b * FB + so, in.bin[b] + go);
+          }
         }
       }
     }
@@ -702,7 +712,8 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     if (Est::kNb > 0 && it < ntiles) {
       const int t0 = seg_lo + (BWD ? ntiles - 1 - it : it) * S::TILE + c * L;
       const int tn = BWD ? t0 + L : t0 - 1;
-      if (row_ok && t0 < seg_hi && tn >= 0 && tn < g.T) est.nb_load(lay, row, tn, got);
+      if (row_ok && t0 < seg_hi && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T))
+        est.nb_load(lay, row, tn, got);
     }
   };
 
@@ -731,7 +742,7 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     const int n = (row_ok && t0 < seg_hi) ? L : 0;
     const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
     const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
-                           (uint32_t)t0 * E32 + (uint32_t)row, E32};
+                           (uint32_t)t0 * E32 + (uint32_t)row, E32, E32 * (uint32_t)g.T};
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
@@ -796,10 +807,227 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
     est.template store<L>(R, io);
   }
-  if (agg_mode && cs == 0 && row0 + js < g.E)
+  if (agg_mode && cs == 0 && row0 + js < g.E && in_range((row0 + js) * g.nseg + seg, g.E * (int64_t)g.nseg))
     reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
 
+// ---------------------------------------------------------------------------
+// bulk time-major driver: the staged driver's tile loop with each tile's
+// inputs moved by the tensor memory accelerator.  Preconditions (checked by
+// the planner): T % 8 == 0, E * T < 2^32, E % 16 == 0, 16-byte aligned
+// inputs, one 2-D tensor map per staged input (TmaSet, encoded on the host).
+// Per tile and input, thread 0 issues one cp.async.bulk.tensor copy of the
+// [TILE, EW] block into a ring of NS stages, NS - 1 tiles ahead of the scan;
+// completion is counted in bytes on the stage's mbarrier.  No thread issues
+// per-element copies, so the bytes in flight are set by the ring, not by
+// registers or occupancy.  Every wait is bounded (mbar_wait_bounded): a
+// copy that never lands sets the status word and the CTA returns.
+// ---------------------------------------------------------------------------
+#ifndef RLCA_TB_STAGES
+#define RLCA_TB_STAGES 2
+#endif
+template <int EW, int CT>
+struct TbShape : TfShape<EW, CT> {
+  static constexpr int NS = RLCA_TB_STAGES;
+  static constexpr int CS = TfShape<EW, CT>::L * EW;  // chunk stride in a stage buffer: [TILE][EW], dense
+  static constexpr int FB = CT * CS;                  // elements per staged buffer (= TILE * EW)
+  static_assert(EW == 16 || EW == 32, "16-byte rows of flags: at least 16 environments");
+};
+template <class Est, int EW, int CT>
+__host__ __device__ constexpr size_t tb_stage_bytes() {
+  // FB * element size is a multiple of 128 for EW >= 16, so every buffer
+  // starts on a 128-byte boundary
+  return (size_t)TbShape<EW, CT>::FB * (sizeof(typename Est::Store) * Est::kSF + Est::kSB);
+}
+template <class Est, int EW, int CT>
+__host__ __device__ constexpr size_t tb_smem_bytes() {
+  // barriers (128 B), exchange arrays, up to 128 B of alignment slack, ring
+  return 128 + align16(tf_smem_bytes<typename Est::V, EW, CT>()) + 128 +
+         TbShape<EW, CT>::NS * tb_stage_bytes<Est, EW, CT>();
+}
 
+template <class Est, int EW, int CT>
+__global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, TbShape<EW, CT>::BLOCK>()))
+    tm_bulk_kernel(Est est, Geom g, const __grid_constant__ TmaSet maps) {
+  using S = TbShape<EW, CT>;
+  using V = typename Est::V;
+  constexpr bool BWD = Est::kBackward;
+  using ST = typename Est::Store;
+  constexpr int L = S::L, PAD = S::PAD, NS = S::NS, CS = S::CS, FB = S::FB;
+  constexpr int ES = (int)sizeof(ST);
+  constexpr size_t STAGE = tb_stage_bytes<Est, EW, CT>();
+  constexpr size_t FLAGS_AT = (size_t)ES * Est::kSF * FB;  // flag buffers' offset in a stage
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);         // [NS] stage barriers
+  int* abort_flag = reinterpret_cast<int*>(smem + 8 * NS);    // set by a wait that gave up
+  Aff<V>* xs = reinterpret_cast<Aff<V>*>(smem + 128);        // [CT][PAD] chunk maps
+  V* ys = reinterpret_cast<V*>(xs + CT * PAD);                // [CT][PAD] values entering each chunk
+  const uintptr_t rb = reinterpret_cast<uintptr_t>(smem + 128 + align16(tf_smem_bytes<V, EW, CT>()));
+  unsigned char* ring = reinterpret_cast<unsigned char*>((rb + 127) & ~uintptr_t(127));
+
+  const int tid = threadIdx.x;
+  const int j = tid % EW, c = tid / EW;    // load / emit role
+  const int js = tid / CT, cs = tid % CT;  // scan role
+  const int seg = g.nseg == 1 ? 0 : (int)(blockIdx.x % (unsigned)g.nseg);
+  const int64_t row0 = (int64_t)(g.nseg == 1 ? blockIdx.x : blockIdx.x / (unsigned)g.nseg) * EW;
+  const int64_t row = row0 + j;
+  const bool row_ok = row < g.E;
+  const int seg_lo = seg * g.seg_len;
+  const int seg_hi = min(g.T, seg_lo + g.seg_len);
+  const bool agg_mode = g.mode == kModeAggregate;
+  const uint32_t E32 = (uint32_t)g.E;
+  const TimeMajor lay{g.E, g.T};
+  const bool early = g.early != 0 && g.nseg == 1;
+  pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+#pragma unroll
+    for (int b = 0; b < Est::kSF; ++b) tma_prefetch_map(&maps.f[b]);
+  }
+  if (!early) pdl_wait();
+  __syncthreads();
+
+  StagedList in;
+  est.staged_io(in);
+  const int ntiles = (seg_hi - seg_lo + S::TILE - 1) / S::TILE;
+  int nflags = 0;
+#pragma unroll
+  for (int b = 0; b < Est::kSB; ++b) nflags += in.bin[b] != nullptr ? 1 : 0;
+  const uint32_t tx_bytes = (uint32_t)(S::TILE * EW) * (uint32_t)(ES * Est::kSF + nflags);
+
+  // thread 0: the copies of the it-th tile in processing order into stage it % NS
+  auto issue = [&](int it) {
+    if (it >= ntiles) return;
+    const int ts = seg_lo + (BWD ? ntiles - 1 - it : it) * S::TILE;
+    unsigned char* st = ring + (size_t)(it % NS) * STAGE;
+    uint64_t* bar = &bars[it % NS];
+    mbar_arrive_expect_tx(bar, tx_bytes);
+#pragma unroll
+    for (int b = 0; b < Est::kSF; ++b) tma_load_2d(st + (size_t)b * FB * ES, &maps.f[b], (int)row0, ts, bar);
+#pragma unroll
+    for (int b = 0; b < Est::kSB; ++b)
+      if (in.bin[b] != nullptr) tma_load_2d(st + FLAGS_AT + (size_t)b * FB, &maps.b[b], (int)row0, ts, bar);
+  };
+  // thread 0, after a wait gave up: let the copies already issued land (each
+  // wait bounded again) before the CTA exits
+  auto drain = [&](int from) {
+    for (int k = from; k < ntiles && k < from + NS; ++k) mbar_wait_bounded(&bars[k % NS], (uint32_t)(k / NS) & 1u);
+  };
+
+  // the neighbour step's inputs of the it-th tile, loaded one tile ahead
+  constexpr int NB = Est::kNb > 0 ? Est::kNb : 1;
+  auto nb_fetch = [&](int it, float (&got)[NB]) {
+#pragma unroll
+    for (int i = 0; i < NB; ++i) got[i] = 0.f;
+    if (Est::kNb > 0 && it < ntiles) {
+      const int t0 = seg_lo + (BWD ? ntiles - 1 - it : it) * S::TILE + c * L;
+      const int tn = BWD ? t0 + L : t0 - 1;
+      if (row_ok && t0 < seg_hi && tn >= 0 && tn < g.T && in_range(lay.at(row, tn), g.E * (int64_t)g.T))
+        est.nb_load(lay, row, tn, got);
+    }
+  };
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s) issue(s);
+  }
+  float nb_cur[NB];
+  nb_fetch(0, nb_cur);
+
+  // scan role: the value entering this segment (full pass) or the map of
+  // the whole segment (first pass of the two-pass path)
+  V carry = V(0);
+  Aff<V> seg_map = aff_identity<V>();
+  if (!agg_mode && row0 + js < g.E) {
+    carry = est.row_carry(row0 + js);
+    if (g.nseg > 1) carry = segment_carry_in<V, BWD>(g, row0 + js, seg, carry);
+  }
+  for (int it = 0; it < ntiles; ++it) {
+    // stage (it - 1) % NS was last read before the first barrier of iteration it - 1
+    if (tid == 0) issue(it + NS - 1);
+    float nb_nxt[NB];
+    nb_fetch(it + 1, nb_nxt);
+    const int tile = BWD ? ntiles - 1 - it : it;
+    const int ts = seg_lo + tile * S::TILE;
+    const int t0 = ts + c * L;
+    const int n = (row_ok && t0 < seg_hi) ? L : 0;
+    const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
+    if (!mbar_wait_bounded(&bars[it % NS], (uint32_t)(it / NS) & 1u)) *abort_flag = 1;
+    const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
+                               (uint32_t)t0 * E32 + (uint32_t)row, E32, E32 * (uint32_t)g.T};
+
+    typename Est::template Regs<L> R;
+    est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
+    if constexpr (Est::kNb > 0) est.nb_take(R, nb_cur);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) nb_cur[i] = nb_nxt[i];
+
+    Aff<V> cf[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) cf[k] = n != 0 ? est.coef(R, k, t0 + k) : aff_identity<V>();
+    Aff<V> agg = aff_identity<V>();
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) agg = compose(cf[k], agg);
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) agg = compose(cf[k], agg);
+    }
+    xs[c * PAD + j] = agg;
+    __syncthreads();
+    if (*abort_flag != 0) {  // uniform: read after the barrier by every thread
+      if (tid == 0) drain(it);
+      return;
+    }
+
+    Aff<V> m = xs[cs * PAD + js];
+#pragma unroll
+    for (int d = 1; d < CT; d <<= 1) {
+      if (BWD) {
+        const Aff<V> o = shfl_down_aff(m, d, CT);
+        if (cs + d < CT) m = compose(m, o);
+      } else {
+        const Aff<V> o = shfl_up_aff(m, d, CT);
+        if (cs >= d) m = compose(m, o);
+      }
+    }
+    Aff<V> ex = BWD ? shfl_down_aff(m, 1, CT) : shfl_up_aff(m, 1, CT);
+    if (cs == (BWD ? CT - 1 : 0)) ex = aff_identity<V>();
+    const Aff<V> tot = shfl_idx_aff(m, BWD ? 0 : CT - 1, CT);
+    if (agg_mode) {
+      seg_map = compose(tot, seg_map);  // tiles arrive in the order the recurrence applies them
+    } else {
+      ys[cs * PAD + js] = ex.a + ex.b * carry;
+      carry = tot.a + tot.b * carry;
+    }
+    __syncthreads();
+    if (agg_mode) continue;
+
+    V A = ys[c * PAD + j];
+    if (BWD) {
+#pragma unroll
+      for (int k = L - 1; k >= 0; --k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        V adj = A;
+        A = cf[k].a + cf[k].b * A;
+        est.emit(R, k, A, adj, cf[k]);
+      }
+    }
+    if (early && it == 0) pdl_wait();  // the previous kernel may still read or write what we overwrite
+    est.template store<L>(R, io);
+  }
+  if (agg_mode && cs == 0 && row0 + js < g.E && in_range((row0 + js) * g.nseg + seg, g.E * (int64_t)g.nseg))
+    reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
+}
 
 }  // namespace rlca

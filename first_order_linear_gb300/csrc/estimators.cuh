@@ -68,9 +68,11 @@ __device__ __forceinline__ void load_boundary(const BoundaryArgs& b, BoundaryReg
   if (HAS_TRUNC && R.trunc != 0u) {  // truncations are rare: one branch instead of L predicated loads
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if ((R.trunc >> k) & 1u) R.tv[k] = Stor<ST>::ld(b.tv, io.at(k));
+      if (((R.trunc >> k) & 1u) && in_range(io.at(k), io.total())) R.tv[k] = Stor<ST>::ld(b.tv, io.at(k));
   }
-  R.boot = (io.n > 0 && io.t0 + io.n == b.T && b.boot != nullptr) ? Stor<ST>::ld(b.boot, io.row) : 0.f;
+  R.boot = (io.n > 0 && io.t0 + io.n == b.T && b.boot != nullptr && in_range(io.row, io.envs()))
+               ? Stor<ST>::ld(b.boot, io.row)
+               : 0.f;
 }
 
 template <class F>
@@ -485,6 +487,7 @@ struct RetraceStage {
   const int32_t* act;
   int A;
   float lambda;
+  int64_t items;  // E * T steps (read by the index-check build)
 
   struct Pending {
     int at;
@@ -523,6 +526,7 @@ struct RetraceStage {
   // once and committed as one group (the shared buffers start on 16-byte
   // boundaries); the taken action and mu(a_t) load into registers alongside
   __device__ __forceinline__ Pending issue(int64_t e0, int cnt, int lane, float* raw_q, float* raw_p) const {
+    if (!span_in_range(e0, cnt, items)) cnt = 0;  // index-check build: skip the block
     const unsigned char* qb = reinterpret_cast<const unsigned char*>(q) + e0 * A * ES;
     const unsigned char* pb = reinterpret_cast<const unsigned char*>(pi) + e0 * A * ES;
     copy_block(reinterpret_cast<unsigned char*>(raw_q), reinterpret_cast<unsigned char*>(raw_p), qb, pb,
@@ -544,8 +548,8 @@ struct RetraceStage {
   // scalars at index `slot` of the dst arrays
   __device__ __forceinline__ void finish(const Pending& pd, int cnt, int lane, const float* raw_q,
                                          const float* raw_p, float* dst_ev, float* dst_qa, float* dst_c,
-                                         int slot) const {
-    if (lane < cnt) {
+                                         int slot, int nslots) const {
+    if (lane < cnt && in_range(slot, nslots)) {
       const int base = lane * A;
       float ev = 0.f;
       if constexpr (ES == 4) {
@@ -584,7 +588,7 @@ struct RetraceStage {
   // chunk's copies are issued before waiting on the current one.
   template <int NBUF, class Where>
   __device__ __forceinline__ void walk(int nch, int warp, int NW, int lane, float* raw, float* s_ev, float* s_qa,
-                                       float* s_c, Where where) const {
+                                       float* s_c, int nslots, Where where) const {
     const int blk = 32 * A;
     auto buf = [&](int k) { return raw + (NBUF == 2 ? (k & 1) : 0) * 2 * blk; };
     int64_t e0 = 0;
@@ -610,7 +614,7 @@ struct RetraceStage {
           cp_async_wait<0>();
         }
         __syncwarp();
-        if (cur_ok) finish(cur, cnt, lane, buf(k), buf(k) + blk, s_ev, s_qa, s_c, slot);
+        if (cur_ok) finish(cur, cnt, lane, buf(k), buf(k) + blk, s_ev, s_qa, s_c, slot, nslots);
         __syncwarp();
         cur = nxt;
         cur_ok = nx_ok;
@@ -622,7 +626,7 @@ struct RetraceStage {
         const Pending pd = issue(e0, cnt, lane, raw, raw + blk);
         cp_async_wait<0>();
         __syncwarp();
-        finish(pd, cnt, lane, raw, raw + blk, s_ev, s_qa, s_c, slot);
+        finish(pd, cnt, lane, raw, raw + blk, s_ev, s_qa, s_c, slot, nslots);
         __syncwarp();
       }
     }
@@ -671,7 +675,7 @@ struct RetraceEst {
     if (g.aux != nullptr && g.mode == kModeFull) {
       for (int i = threadIdx.x; i < ROWS * nst; i += BLOCK) {
         const int rr = i / nst, k = i - rr * nst;
-        if (row0 + rr < lay.E) {
+        if (row0 + rr < lay.E && in_range(lay.at(row0 + rr, ts + k), plane)) {
           const int64_t gi = lay.at(row0 + rr, ts + k);
           s_ev[rr * SROW + k] = g.aux[gi];
           s_qa[rr * SROW + k] = g.aux[plane + gi];
@@ -682,7 +686,7 @@ struct RetraceEst {
       return;
     }
     const int per_row = (nst + 31) / 32;
-    st.template walk<retrace_bufs(false)>(ROWS * per_row, warp, NW, lane, raw, s_ev, s_qa, s_c,
+    st.template walk<retrace_bufs(false)>(ROWS * per_row, warp, NW, lane, raw, s_ev, s_qa, s_c, ROWS * SROW,
             [&](int ch, int64_t* e0, int* cnt, int* slot) {
               const int rr = ch / per_row, m = ch - rr * per_row;
               if (row0 + rr >= lay.E) return false;
@@ -697,7 +701,7 @@ struct RetraceEst {
       const int own = te - ts;
       for (int i = threadIdx.x; i < ROWS * own; i += BLOCK) {
         const int rr = i / own, k = i - rr * own;
-        if (row0 + rr < lay.E) {
+        if (row0 + rr < lay.E && in_range(lay.at(row0 + rr, ts + k), plane)) {
           const int64_t gi = lay.at(row0 + rr, ts + k);
           g.aux[gi] = s_ev[rr * SROW + k];
           g.aux[plane + gi] = s_qa[rr * SROW + k];
@@ -725,7 +729,7 @@ struct RetraceEst {
     if (g.aux != nullptr && g.mode == kModeFull) {
       for (int i = threadIdx.x; i < nst * 32; i += BLOCK) {
         const int k = i >> 5, l = i & 31;
-        if (l < cnt) {
+        if (l < cnt && in_range(lay.at(row0 + l, ts + k), plane) && in_range(i, SROWS * 32)) {
           const int64_t gi = lay.at(row0 + l, ts + k);
           s_ev[i] = g.aux[gi];
           s_qa[i] = g.aux[plane + gi];
@@ -735,7 +739,7 @@ struct RetraceEst {
       __syncthreads();
       return;
     }
-    st.template walk<retrace_bufs(true)>(nst, warp, NW, lane, raw, s_ev, s_qa, s_c, [&](int i, int64_t* e0, int* c, int* slot) {
+    st.template walk<retrace_bufs(true)>(nst, warp, NW, lane, raw, s_ev, s_qa, s_c, SROWS * 32, [&](int i, int64_t* e0, int* c, int* slot) {
       *e0 = lay.at(row0, ts + i);
       *c = cnt;
       *slot = i * 32 + lane;
@@ -745,7 +749,7 @@ struct RetraceEst {
     if (g.aux != nullptr) {  // first pass: steps ts .. te-1 are this tile's own
       for (int i = threadIdx.x; i < (te - ts) * 32; i += BLOCK) {
         const int k = i >> 5, l = i & 31;
-        if (l < cnt) {
+        if (l < cnt && in_range(lay.at(row0 + l, ts + k), plane) && in_range(i, SROWS * 32)) {
           const int64_t gi = lay.at(row0 + l, ts + k);
           g.aux[gi] = s_ev[i];
           g.aux[plane + gi] = s_qa[i];
@@ -771,9 +775,9 @@ struct RetraceEst {
 #pragma unroll
     for (int k = 0; k < L; ++k) {
       const int t = t0 + k + 1;  // successor step
-      if (k < n && t < b.T) {
-        const int i = t - ts;
-        const int idx = kTM ? i * 32 + slot : slot * srows + i;
+      const int i = t - ts;
+      const int idx = kTM ? i * 32 + slot : slot * srows + i;
+      if (k < n && t < b.T && in_range(idx, plane)) {
         R.evn[k] = s_ev[idx];
         R.qan[k] = s_qa[idx];
         R.cn[k] = s_c[idx];

@@ -26,6 +26,7 @@ struct Plan {
   bool fast;        // env-major, one tile per row, one segment (em_fast_kernel)
   bool tm_fast;     // time-major, T % 8 == 0, E * T < 2^32, one segment (tm_fast_kernel)
   bool tm_staged;   // ... and inputs staged through shared memory (tm_staged_kernel)
+  bool tm_bulk;     // ... staged by tensor-memory-accelerator tile copies (tm_bulk_kernel)
   int steps;        // steps per thread of the fast driver (kEmSteps or 8)
   int width;        // env-major: threads per row; time-major: chunk-threads per environment
   int env_width;    // fast time-major: environments per CTA (8 or 32)
@@ -47,8 +48,39 @@ constexpr size_t aux_offset(size_t ws_bytes, size_t aux_bytes) { return ws_bytes
 
 // Fills *p for a problem; returns false when the sizes cannot be launched.
 // vec: the env-major arrays are 16-byte aligned (4-byte for flags) and
-// T % 4 == 0, so rows can be read as 16-byte vectors.
-bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec, Plan* p);
+// T % 4 == 0, so rows can be read as 16-byte vectors.  bulk: every staged
+// input starts on a 16-byte boundary, E % 16 == 0 and the tensor-map encoder
+// is available, so time-major tiles may move by tensor copies.
+bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec, Plan* p,
+               bool bulk = false);
+
+// bytes a time-major step stages per staged input set (float inputs of
+// fbytes each, flag inputs of one byte)
+struct StageCounts {
+  int nf, nb;
+};
+StageCounts stage_counts(Kind kind);
+
+// The 2-D tensor maps of a call's staged time-major inputs ([T, E], E
+// innermost; tiles of ew environments x rows steps).  False when the
+// encoder is unavailable or refuses a map.
+bool encode_tm_maps(const StagedList& in, int elem_bytes, int64_t E, int64_t T, int ew, int rows, TmaSet* out);
+// whether encode_tm_maps can work at all (the driver's encoder was found)
+bool tensor_maps_available();
+
+// RLCA_OK, or in the index-check build RLCA_ERR_CUDA once the stream's work
+// has recorded a condition in a status word (it synchronises the stream)
+int checked_build_status(cudaStream_t s);
+
+// Reads (and with clear, zeroes) the device status word of each kernel
+// translation unit, ORed into *word.  Synchronous copies.
+cudaError_t status_values(unsigned int* word, bool clear);
+cudaError_t status_values_bf16_a(unsigned int* word, bool clear);
+cudaError_t status_values_bf16_b(unsigned int* word, bool clear);
+cudaError_t status_offpolicy(unsigned int* word, bool clear);
+cudaError_t status_offpolicy_bf16(unsigned int* word, bool clear);
+cudaError_t status_forward(unsigned int* word, bool clear);
+cudaError_t status_forward_bf16(unsigned int* word, bool clear);
 
 #ifndef RLCA_TM_STAGED
 #define RLCA_TM_STAGED 1
@@ -62,6 +94,27 @@ constexpr bool kTmStaged = RLCA_TM_STAGED != 0;
 // ... also for float32 tiles of 16 environments (rows of 64 bytes) where the
 // direct driver would take 8
 constexpr bool kTmStaged16 = RLCA_TM_STAGED16 != 0;
+#ifndef RLCA_TM_BULK
+#define RLCA_TM_BULK 1
+#endif
+// build-time choice: time-major tiles move by tensor copies (tm_bulk_kernel)
+// where the inputs allow it
+constexpr bool kTmBulk = RLCA_TM_BULK != 0;
+#ifndef RLCA_TB_RING_BYTES
+#define RLCA_TB_RING_BYTES (96 * 1024)
+#endif
+// shared memory the bulk driver's ring may take (two CTAs an SM)
+constexpr size_t kTbRingBytes = RLCA_TB_RING_BYTES;
+#ifndef RLCA_TB_CTAS_PER_SM
+#define RLCA_TB_CTAS_PER_SM 2
+#endif
+// CTAs per SM below which the bulk driver splits rows into segments
+constexpr int kTbCtasPerSm = RLCA_TB_CTAS_PER_SM;
+#ifndef RLCA_TB_MIN_ENVS_PER_SM
+#define RLCA_TB_MIN_ENVS_PER_SM 64
+#endif
+// environments per SM from which time-major calls take the bulk driver
+constexpr int kTbMinEnvsPerSm = RLCA_TB_MIN_ENVS_PER_SM;
 
 // Launches the scan of one estimator functor (both passes of the two-pass
 // path when p.nseg > 1).  Defined by explicit instantiation in the family

@@ -27,6 +27,8 @@ struct GIO {
   __device__ __forceinline__ bool vec() const { return VEC_CT || vec_rt; }
 
   __device__ __forceinline__ int64_t at(int k) const { return lay.at(row, t0 + k); }
+  __device__ __forceinline__ int64_t total() const { return lay.E * (int64_t)lay.T; }
+  __device__ __forceinline__ int64_t envs() const { return lay.E; }
   template <int L>
   __device__ __forceinline__ void f(int, const float* p, float (&o)[L]) const {
     load_vals<L, Lay, ST>(p, lay, row, t0, n, vec(), o);
@@ -61,38 +63,43 @@ struct TmIO32 {
   int n;
   uint32_t off;  // t0 * E + row
   uint32_t E;
+  uint32_t tot;  // E * T (read by the index-check build)
 
   __device__ __forceinline__ uint32_t o(int k) const { return off + (uint32_t)k * E; }
   __device__ __forceinline__ int64_t at(int k) const { return (int64_t)o(k); }
+  __device__ __forceinline__ int64_t total() const { return tot; }
+  __device__ __forceinline__ int64_t envs() const { return E; }
   template <int L>
   __device__ __forceinline__ void f(int, const float* __restrict__ p, float (&v)[L]) const {
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? Stor<ST>::ld(p, o(k)) : 0.f;
+    for (int k = 0; k < L; ++k) v[k] = (n != 0 && in_range(o(k), tot)) ? Stor<ST>::ld(p, o(k)) : 0.f;
   }
   template <int L>
   __device__ __forceinline__ void i(int, const int32_t* __restrict__ p, uint32_t (&v)[L]) const {
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? (uint32_t)__ldg(p + o(k)) : 0u;
+    for (int k = 0; k < L; ++k) v[k] = (n != 0 && in_range(o(k), tot)) ? (uint32_t)__ldg(p + o(k)) : 0u;
   }
   template <int L>
   __device__ __forceinline__ uint32_t flags(int, const uint8_t* __restrict__ p) const {
     if (p == nullptr || n == 0) return 0u;
     uint32_t bits = 0u;
 #pragma unroll
-    for (int k = 0; k < L; ++k) bits |= (uint32_t)(__ldg(p + o(k)) != 0) << k;
+    for (int k = 0; k < L; ++k) bits |= (uint32_t)(in_range(o(k), tot) && __ldg(p + o(k)) != 0) << k;
     return bits;
   }
   template <int L>
   __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) Stor<ST>::st(p, o(k), v[k]);
+    for (int k = 0; k < L; ++k)
+      if (in_range(o(k), tot)) Stor<ST>::st(p, o(k), v[k]);
   }
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) p[o(k)] = (int32_t)v[k];
+    for (int k = 0; k < L; ++k)
+      if (in_range(o(k), tot)) p[o(k)] = (int32_t)v[k];
   }
 };
 
@@ -112,21 +119,24 @@ struct TmSIO {
   int n;
   uint32_t off;  // t0 * E + row
   uint32_t E;
+  uint32_t tot;  // E * T (read by the index-check build)
 
   __device__ __forceinline__ uint32_t o(int k) const { return off + (uint32_t)k * E; }
   __device__ __forceinline__ int64_t at(int k) const { return (int64_t)o(k); }
+  __device__ __forceinline__ int64_t total() const { return tot; }
+  __device__ __forceinline__ int64_t envs() const { return E; }
   template <int L>
   __device__ __forceinline__ void f(int idx, const float*, float (&v)[L]) const {
     const ST* s = fbuf + idx * FB + slot;
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? static_cast<float>(s[k * EW]) : 0.f;
+    for (int k = 0; k < L; ++k) v[k] = (n != 0 && in_range(slot + k * EW, FB)) ? static_cast<float>(s[k * EW]) : 0.f;
   }
   template <int L>
   __device__ __forceinline__ void i(int idx, const int32_t*, uint32_t (&v)[L]) const {
     static_assert(sizeof(ST) == 4, "int inputs are staged as 4-byte elements");
     const uint32_t* s = reinterpret_cast<const uint32_t*>(fbuf + idx * FB + slot);
 #pragma unroll
-    for (int k = 0; k < L; ++k) v[k] = n != 0 ? s[k * EW] : 0u;
+    for (int k = 0; k < L; ++k) v[k] = (n != 0 && in_range(slot + k * EW, FB)) ? s[k * EW] : 0u;
   }
   template <int L>
   __device__ __forceinline__ uint32_t flags(int idx, const uint8_t* p) const {
@@ -134,20 +144,22 @@ struct TmSIO {
     const uint8_t* s = bbuf + idx * FB + slot;
     uint32_t bits = 0u;
 #pragma unroll
-    for (int k = 0; k < L; ++k) bits |= (uint32_t)(s[k * EW] != 0) << k;
+    for (int k = 0; k < L; ++k) bits |= (uint32_t)(in_range(slot + k * EW, FB) && s[k * EW] != 0) << k;
     return bits;
   }
   template <int L>
   __device__ __forceinline__ void put(int, float* __restrict__ p, const float (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) Stor<ST>::st(p, o(k), v[k]);
+    for (int k = 0; k < L; ++k)
+      if (in_range(o(k), tot)) Stor<ST>::st(p, o(k), v[k]);
   }
   template <int L>
   __device__ __forceinline__ void put_i(int, int32_t* __restrict__ p, const uint32_t (&v)[L]) const {
     if (p == nullptr || n == 0) return;
 #pragma unroll
-    for (int k = 0; k < L; ++k) p[o(k)] = (int32_t)v[k];
+    for (int k = 0; k < L; ++k)
+      if (in_range(o(k), tot)) p[o(k)] = (int32_t)v[k];
   }
 };
 

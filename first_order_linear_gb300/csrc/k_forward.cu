@@ -10,4 +10,5 @@ template cudaError_t run_scan<PrefixSumEst<float>>(const PrefixSumEst<float>&, c
                                                    cudaStream_t);
 template cudaError_t run_scan<AffineEst<true>>(const AffineEst<true>&, const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<AffineEst<false>>(const AffineEst<false>&, const Plan&, const Geom&, cudaStream_t);
+cudaError_t status_forward(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

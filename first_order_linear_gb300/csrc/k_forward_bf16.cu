@@ -9,4 +9,5 @@ template cudaError_t run_scan<AffineEst<true, bf16>>(const AffineEst<true, bf16>
     const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<AffineEst<false, bf16>>(const AffineEst<false, bf16>&,
     const Plan&, const Geom&, cudaStream_t);
+cudaError_t status_forward_bf16(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

@@ -7,4 +7,5 @@ template cudaError_t run_scan<VtraceEst<false>>(const VtraceEst<false>&, const P
 template cudaError_t run_scan<RetraceEst<true>>(const RetraceEst<true>&, const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<RetraceEst<false>>(const RetraceEst<false>&, const Plan&, const Geom&,
                                                  cudaStream_t);
+cudaError_t status_offpolicy(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

@@ -10,4 +10,5 @@ template cudaError_t run_scan<RetraceEst<true, bf16>>(const RetraceEst<true, bf1
                                                      cudaStream_t);
 template cudaError_t run_scan<RetraceEst<false, bf16>>(const RetraceEst<false, bf16>&, const Plan&, const Geom&,
                                                       cudaStream_t);
+cudaError_t status_offpolicy_bf16(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

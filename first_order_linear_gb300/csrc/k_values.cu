@@ -14,4 +14,5 @@ template cudaError_t run_scan<ValueTargetsEst<true>>(const ValueTargetsEst<true>
                                                      cudaStream_t);
 template cudaError_t run_scan<ValueTargetsEst<false>>(const ValueTargetsEst<false>&, const Plan&, const Geom&,
                                                       cudaStream_t);
+cudaError_t status_values(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

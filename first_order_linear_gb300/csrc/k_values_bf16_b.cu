@@ -10,4 +10,5 @@ template cudaError_t run_scan<ValueTargetsEst<true, bf16>>(const ValueTargetsEst
     const Plan&, const Geom&, cudaStream_t);
 template cudaError_t run_scan<ValueTargetsEst<false, bf16>>(const ValueTargetsEst<false, bf16>&,
     const Plan&, const Geom&, cudaStream_t);
+cudaError_t status_values_bf16_b(unsigned int* word, bool clear) { return tu_status(word, clear); }
 }  // namespace rlca

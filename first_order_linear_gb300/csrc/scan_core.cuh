@@ -32,6 +32,38 @@ namespace rlca {
 constexpr unsigned kFullMask = 0xffffffffu;
 
 // ---------------------------------------------------------------------------
+// device status word and the index-check build.  Each translation unit has
+// its own word (internal linkage); the host reads them with
+// rlca_device_status.  A kernel records a condition here instead of
+// trapping: a bounded wait that gave up, or (built with RLCA_INDEX_CHECK) an
+// index outside its array, whose access is then skipped or clamped.
+// ---------------------------------------------------------------------------
+static __device__ unsigned int g_tu_status;
+constexpr unsigned int kStatusWaitTimeout = 1u;
+constexpr unsigned int kStatusIndex = 2u;
+#ifdef RLCA_INDEX_CHECK
+constexpr bool kIndexCheck = true;
+#else
+constexpr bool kIndexCheck = false;
+#endif
+// 0 <= i < n; in the index-check build a miss is recorded (the caller skips
+// the access); otherwise always true and free
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n) {
+  if constexpr (kIndexCheck) {
+    if (i < 0 || i >= n) {
+      atomicOr(&g_tu_status, kStatusIndex);
+      return false;
+    }
+  }
+  return true;
+}
+// [i, i + len) inside [0, n)
+__device__ __forceinline__ bool span_in_range(int64_t i, int64_t len, int64_t n) {
+  if constexpr (kIndexCheck) return in_range(i, n) && in_range(i + len - 1, n);
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // storage of the floating-point arrays.  Arithmetic and the scan state are
 // float32 always; with RLCA_BF16 every float array of a call holds bfloat16
 // (the upper half of a float32), converted on load and rounded to nearest
@@ -182,29 +214,34 @@ struct TimeMajor {  // [T, E], e fastest
 template <int L, class Lay, class ST = float>
 __device__ __forceinline__ void load_vals(const float* __restrict__ p, const Lay& lay, int64_t row,
                                           int t0, int n, bool vec, float (&out)[L]) {
+  const int64_t tot = lay.E * (int64_t)lay.T;
   if (vec) {
     const int64_t base = lay.at(row, t0);
     if constexpr (sizeof(ST) == 2 && L % 8 == 0) {  // 16-byte vectors of 8 bfloat16 steps
 #pragma unroll
-      for (int i = 0; i < L / 8; ++i) Stor<ST>::ld8(p, base + 8 * i, 8 * i < n, &out[8 * i]);
+      for (int i = 0; i < L / 8; ++i)
+        Stor<ST>::ld8(p, base + 8 * i, 8 * i < n && span_in_range(base + 8 * i, 8, tot), &out[8 * i]);
     } else {
 #pragma unroll
-      for (int i = 0; i < L / 4; ++i) Stor<ST>::ld4(p, base + 4 * i, 4 * i < n, &out[4 * i]);
+      for (int i = 0; i < L / 4; ++i)
+        Stor<ST>::ld4(p, base + 4 * i, 4 * i < n && span_in_range(base + 4 * i, 4, tot), &out[4 * i]);
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < L; ++k) out[k] = (k < n) ? Stor<ST>::ld(p, lay.at(row, t0 + k)) : 0.f;
+    for (int k = 0; k < L; ++k)
+      out[k] = (k < n && in_range(lay.at(row, t0 + k), tot)) ? Stor<ST>::ld(p, lay.at(row, t0 + k)) : 0.f;
   }
 }
 
 template <int L, class Lay>
 __device__ __forceinline__ void load_ints(const int32_t* __restrict__ p, const Lay& lay, int64_t row,
                                           int t0, int n, bool vec, uint32_t (&out)[L]) {
+  const int64_t tot = lay.E * (int64_t)lay.T;
   if (vec) {
     const int4* q = reinterpret_cast<const int4*>(p + lay.at(row, t0));
 #pragma unroll
     for (int i = 0; i < L / 4; ++i) {
-      int4 v = (4 * i < n) ? __ldg(q + i) : make_int4(0, 0, 0, 0);
+      int4 v = (4 * i < n && span_in_range(lay.at(row, t0) + 4 * i, 4, tot)) ? __ldg(q + i) : make_int4(0, 0, 0, 0);
       out[4 * i + 0] = (uint32_t)v.x;
       out[4 * i + 1] = (uint32_t)v.y;
       out[4 * i + 2] = (uint32_t)v.z;
@@ -212,7 +249,8 @@ __device__ __forceinline__ void load_ints(const int32_t* __restrict__ p, const L
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < L; ++k) out[k] = (k < n) ? (uint32_t)__ldg(p + lay.at(row, t0 + k)) : 0u;
+    for (int k = 0; k < L; ++k)
+      out[k] = (k < n && in_range(lay.at(row, t0 + k), tot)) ? (uint32_t)__ldg(p + lay.at(row, t0 + k)) : 0u;
   }
 }
 
@@ -222,11 +260,12 @@ __device__ __forceinline__ uint32_t load_flags(const uint8_t* __restrict__ p, co
                                                int t0, int n, bool vec) {
   if (p == nullptr) return 0u;
   uint32_t bits = 0u;
+  const int64_t tot = lay.E * (int64_t)lay.T;
   if (vec) {
     const uint32_t* q = reinterpret_cast<const uint32_t*>(p + lay.at(row, t0));
 #pragma unroll
     for (int i = 0; i < L / 4; ++i) {
-      const uint32_t w = (4 * i < n) ? __ldg(q + i) : 0u;
+      const uint32_t w = (4 * i < n && span_in_range(lay.at(row, t0) + 4 * i, 4, tot)) ? __ldg(q + i) : 0u;
       // one bit per nonzero byte: bytes -> 0/1, then the multiply gathers
       // byte k's bit into bit 24 + k (the partial products never overlap)
       const uint32_t m = __vcmpne4(w, 0u) & 0x01010101u;
@@ -235,7 +274,7 @@ __device__ __forceinline__ uint32_t load_flags(const uint8_t* __restrict__ p, co
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k) {
-      if (k < n && __ldg(p + lay.at(row, t0 + k)) != 0) bits |= 1u << k;
+      if (k < n && in_range(lay.at(row, t0 + k), tot) && __ldg(p + lay.at(row, t0 + k)) != 0) bits |= 1u << k;
     }
   }
   return bits;
@@ -243,43 +282,45 @@ __device__ __forceinline__ uint32_t load_flags(const uint8_t* __restrict__ p, co
 
 template <class Lay>
 __device__ __forceinline__ bool load_flag1(const uint8_t* __restrict__ p, const Lay& lay, int64_t row, int t) {
-  return p != nullptr && __ldg(p + lay.at(row, t)) != 0;
+  return p != nullptr && in_range(lay.at(row, t), lay.E * (int64_t)lay.T) && __ldg(p + lay.at(row, t)) != 0;
 }
 
 template <int L, class Lay, class ST = float>
 __device__ __forceinline__ void store_vals(float* __restrict__ p, const Lay& lay, int64_t row, int t0,
                                            int n, bool vec, const float (&v)[L]) {
+  const int64_t tot = lay.E * (int64_t)lay.T;
   if (vec) {
     const int64_t base = lay.at(row, t0);
     if constexpr (sizeof(ST) == 2 && L % 8 == 0) {
 #pragma unroll
       for (int i = 0; i < L / 8; ++i)
-        if (8 * i < n) Stor<ST>::st8(p, base + 8 * i, &v[8 * i]);
+        if (8 * i < n && span_in_range(base + 8 * i, 8, tot)) Stor<ST>::st8(p, base + 8 * i, &v[8 * i]);
     } else {
 #pragma unroll
       for (int i = 0; i < L / 4; ++i)
-        if (4 * i < n) Stor<ST>::st4(p, base + 4 * i, &v[4 * i]);
+        if (4 * i < n && span_in_range(base + 4 * i, 4, tot)) Stor<ST>::st4(p, base + 4 * i, &v[4 * i]);
     }
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if (k < n) Stor<ST>::st(p, lay.at(row, t0 + k), v[k]);
+      if (k < n && in_range(lay.at(row, t0 + k), tot)) Stor<ST>::st(p, lay.at(row, t0 + k), v[k]);
   }
 }
 
 template <int L, class Lay>
 __device__ __forceinline__ void store_ints(int32_t* __restrict__ p, const Lay& lay, int64_t row, int t0,
                                            int n, bool vec, const uint32_t (&v)[L]) {
+  const int64_t tot = lay.E * (int64_t)lay.T;
   if (vec) {
     int4* q = reinterpret_cast<int4*>(p + lay.at(row, t0));
 #pragma unroll
     for (int i = 0; i < L / 4; ++i)
-      if (4 * i < n)
+      if (4 * i < n && span_in_range(lay.at(row, t0) + 4 * i, 4, tot))
         q[i] = make_int4((int)v[4 * i], (int)v[4 * i + 1], (int)v[4 * i + 2], (int)v[4 * i + 3]);
   } else {
 #pragma unroll
     for (int k = 0; k < L; ++k)
-      if (k < n) p[lay.at(row, t0 + k)] = (int32_t)v[k];
+      if (k < n && in_range(lay.at(row, t0 + k), tot)) p[lay.at(row, t0 + k)] = (int32_t)v[k];
   }
 }
 
@@ -436,10 +477,13 @@ template <class V, bool BWD>
 __device__ __forceinline__ V segment_carry_in(const Geom& g, int64_t row, int seg, V row_carry) {
   V c = row_carry;
   const Aff<V>* ws = reinterpret_cast<const Aff<V>*>(g.ws) + row * g.nseg;
+  const int64_t nmaps = g.E * (int64_t)g.nseg;
   if (BWD) {
-    for (int s = g.nseg - 1; s > seg; --s) c = ws[s].a + ws[s].b * c;
+    for (int s = g.nseg - 1; s > seg; --s)
+      if (in_range(row * g.nseg + s, nmaps)) c = ws[s].a + ws[s].b * c;
   } else {
-    for (int s = 0; s < seg; ++s) c = ws[s].a + ws[s].b * c;
+    for (int s = 0; s < seg; ++s)
+      if (in_range(row * g.nseg + s, nmaps)) c = ws[s].a + ws[s].b * c;
   }
   return c;
 }

@@ -169,5 +169,6 @@ extern "C" int rlca_gae_static_scratch(const float* rewards, const float* values
     est.gamma = gamma; est.gl = gamma * lambda;
     e = run_scan(est, p, g, stream);
   }
-  return e == cudaSuccess ? RLCA_OK : RLCA_ERR_CUDA;
+  if (e != cudaSuccess) return RLCA_ERR_CUDA;
+  return checked_build_status(stream);
 }

@@ -141,6 +141,32 @@ const char *rlca_status_string(int status);
 /* Library version as major*10000 + minor*100 + patch. */
 int rlca_version(void);
 
+/* Device status bits (see rlca_device_status). */
+#define RLCA_STATUS_WAIT_TIMEOUT 0x1u /* a bounded wait on a tile copy gave up */
+#define RLCA_STATUS_INDEX        0x2u /* index-check build: an out-of-range index was skipped */
+
+/*
+ * Device-side status of the kernels launched so far on the CURRENT device:
+ * writes to *status the OR of the status words the kernels keep in device
+ * memory (0: nothing to report), and zeroes them when `clear` is nonzero.
+ * No counterpart in the paper: it reports conditions that a kernel records
+ * instead of trapping.  The only one in the product build is
+ * RLCA_STATUS_WAIT_TIMEOUT: a kernel that waits for its own tensor copies
+ * (the time-major bulk driver) gives up after 0.2 s instead of hanging and
+ * leaves that call's outputs incomplete.  The copies are synchronous: the
+ * call waits for the device's earlier work.  Errors: RLCA_ERR_INVALID_ARG
+ * for a NULL `status`, RLCA_ERR_CUDA when a copy fails.
+ */
+int rlca_device_status(unsigned int *status, int clear);
+
+/* 1 in the index-check build of this library (compiled with
+ * RLCA_INDEX_CHECK: kernels check every index of the staged and two-pass
+ * paths, record a miss as RLCA_STATUS_INDEX instead of trapping, and each
+ * call waits for its kernels, returning RLCA_ERR_CUDA if any recorded a
+ * condition), 0 in the product build.  A debugging aid; no counterpart in
+ * the paper. */
+int rlca_index_checks(void);
+
 /*
  * Bytes of device workspace that the call of `estimator` (RLCA_EST_*) with
  * these sizes and flags needs on the CURRENT device (0 for the one-pass

@@ -44,6 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_host_only_queries(lib):
     assert lib.rlca_version() >= 100
+    assert lib.rlca_device_status(None, 0) == _lib.RLCA_ERR_INVALID_ARG
     assert lib.rlca_status_string(0) == b"ok"
     assert lib.rlca_status_string(1) == b"invalid argument"
     assert lib.rlca_status_string(99) == b"unknown status"

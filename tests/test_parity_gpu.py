@@ -8,6 +8,8 @@ T in {32, 128, 512, 2048}, both layouts, with and without truncation; plus
 edge cases (T = 1, ragged T, tile +- 1, E = 1, misaligned pointers, the
 two-pass path, both flags on one step, int32 wraparound).
 """
+import ctypes as C
+
 import numpy as np
 import pytest
 import torch
@@ -521,3 +523,17 @@ def test_retrace_two_pass_keeps_per_step_scalars():
         rows = parity.sample_rows(E, T, seed=5, n=128)
         want = parity.run_oracle("retrace", d, rows)
         parity.assert_close(parity._np(parity._back(out, tm), rows), want[0], f"retrace two-pass tm={tm}")
+
+
+@pytest.mark.parametrize("kind", ["gae", "vt", "vtrace", "disc", "elig", "psum_i32", "affine_fwd"])
+@pytest.mark.parametrize("E,T", [(9728, 16), (9744, 64), (10240, 520), (16384, 256)])
+def test_time_major_tile_copies_leave_status_clean(cuda_lib, kind, E, T):
+    """Time-major calls with many environments (E >= 64 per SM, E % 16 == 0,
+    16-byte aligned inputs) move their tiles by tensor copies with bounded
+    waits -- 9744 leaves the last CTA's tile half past E, zero-filled; results
+    match the oracle and no wait gives up (the device status word stays 0)."""
+    st = C.c_uint(0)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    parity.check_case(kind, E, T, seed=E + T, time_major=True)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    assert st.value == 0, f"device status {st.value:#x}"
