@@ -1096,9 +1096,12 @@ def run_pages_protocol(args):
     Benchmarking Methodology) on the named configurations: 20 untimed
     calls, then 5 trials of 50 calls, each call alone between two CUDA
     events on its stream; the figure is the smallest of the 5 per-trial
-    medians.  Added here: L2 is flushed before each call (a memset of twice
-    the L2 size, outside the events), so the figure is one isolated launch
-    from a cold L2, nothing overlapped."""
+    medians.  Added here: L2 is flushed before each call, outside the
+    events, by reading a buffer of twice the L2 size (a read leaves clean
+    lines: a memset would leave that much dirty data to be written back
+    during the timed call), so the figure is one isolated launch from a
+    cold L2, nothing overlapped.  ``--pages-flush write`` flushes with a
+    memset instead."""
     import torch
     from first_order_linear_gb300 import build
     build.build()
@@ -1107,7 +1110,8 @@ def run_pages_protocol(args):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     peak, peak_kind = _peaks()
     stream = torch.cuda.Stream(dev)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for kind, E, T, trunc in PAGES_PROTOCOL_CASES:
         d, nbytes, spec = _sweep_case(kind, E, T, trunc, dev)
@@ -1121,7 +1125,10 @@ def run_pages_protocol(args):
             for _ in range(5):
                 ts = []
                 for _ in range(50):
-                    flush.zero_()
+                    if args.pages_flush == "write":
+                        flush.zero_()
+                    else:
+                        torch.sum(flush, dim=0, out=sink)
                     a.record(stream)
                     _sweep_call(kind, d, o, False)
                     b.record(stream)
@@ -1133,7 +1140,8 @@ def run_pages_protocol(args):
                           "us_per_call": round(us, 3), "trial_medians_us": [round(m, 3) for m in medians],
                           "algorithmic_bytes": nbytes, "frac_of_peak": round(nbytes / (us / 1e6) / 1e9 / peak, 4),
                           "peak": f"{peak} GB/s {peak_kind}", "env_steps_per_s": E * T / (us / 1e6),
-                          "timing": "cold L2 (2 x L2 memset before each call), one call between two events, "
+                          "timing": f"cold L2 (2 x L2 {'memset' if args.pages_flush == 'write' else 'read'} "
+                                    "before each call), one call between two events, "
                                     "min over 5 trials of the median of 50"}), flush=True)
         del d, o
         torch.cuda.empty_cache()
@@ -1203,6 +1211,8 @@ def main():
     ap.add_argument("--skip-torch-compile", action="store_true", help="with --torch-baseline: eager only")
     ap.add_argument("--pages-protocol", action="store_true",
                     help="time the named configurations with the paper's protocol (cold L2, isolated calls)")
+    ap.add_argument("--pages-flush", choices=["read", "write"], default="read",
+                    help="with --pages-protocol: flush L2 by reading (default) or by a memset of 2 x L2")
     ap.add_argument("--ncu-case", default="",
                     help="KIND,E,T,em|tm[,bf16]: four calls of one estimator on one batch (a case for ncu), no timing")
     args = ap.parse_args()

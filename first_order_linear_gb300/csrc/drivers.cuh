@@ -1030,4 +1030,6 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
     reinterpret_cast<Aff<V>*>(g.ws)[(row0 + js) * g.nseg + seg] = seg_map;
 }
 
+
+
 }  // namespace rlca

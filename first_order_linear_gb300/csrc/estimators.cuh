@@ -673,13 +673,27 @@ struct RetraceEst {
     const int nst = te - ts + (te < b.T ? 1 : 0);
     const int64_t plane = lay.E * (int64_t)lay.T;
     if (g.aux != nullptr && g.mode == kModeFull) {
-      for (int i = threadIdx.x; i < ROWS * nst; i += BLOCK) {
+      // every load of the tile in flight at once, then the shared-memory writes
+      constexpr int PER = (ROWS * SROW + BLOCK - 1) / BLOCK;
+      float ev[PER], qa[PER], cc[PER];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int i = threadIdx.x + u * BLOCK;
         const int rr = i / nst, k = i - rr * nst;
-        if (row0 + rr < lay.E && in_range(lay.at(row0 + rr, ts + k), plane)) {
-          const int64_t gi = lay.at(row0 + rr, ts + k);
-          s_ev[rr * SROW + k] = g.aux[gi];
-          s_qa[rr * SROW + k] = g.aux[plane + gi];
-          s_c[rr * SROW + k] = g.aux[2 * plane + gi];
+        const bool ok = i < ROWS * nst && row0 + rr < lay.E && in_range(lay.at(row0 + rr, ts + k), plane);
+        const int64_t gi = ok ? lay.at(row0 + rr, ts + k) : 0;
+        ev[u] = ok ? __ldg(g.aux + gi) : 0.f;
+        qa[u] = ok ? __ldg(g.aux + plane + gi) : 0.f;
+        cc[u] = ok ? __ldg(g.aux + 2 * plane + gi) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int i = threadIdx.x + u * BLOCK;
+        const int rr = i / nst, k = i - rr * nst;
+        if (i < ROWS * nst && row0 + rr < lay.E) {
+          s_ev[rr * SROW + k] = ev[u];
+          s_qa[rr * SROW + k] = qa[u];
+          s_c[rr * SROW + k] = cc[u];
         }
       }
       __syncthreads();
@@ -727,13 +741,28 @@ struct RetraceEst {
     const int cnt = (int)min((int64_t)32, lay.E - row0);
     const int64_t plane = lay.E * (int64_t)lay.T;
     if (g.aux != nullptr && g.mode == kModeFull) {
-      for (int i = threadIdx.x; i < nst * 32; i += BLOCK) {
+      // every load of the tile in flight at once, then the shared-memory
+      // writes (one round trip instead of one per loop pass)
+      constexpr int PER = (SROWS * 32 + BLOCK - 1) / BLOCK;
+      float ev[PER], qa[PER], cc[PER];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int i = threadIdx.x + u * BLOCK;
         const int k = i >> 5, l = i & 31;
-        if (l < cnt && in_range(lay.at(row0 + l, ts + k), plane) && in_range(i, SROWS * 32)) {
-          const int64_t gi = lay.at(row0 + l, ts + k);
-          s_ev[i] = g.aux[gi];
-          s_qa[i] = g.aux[plane + gi];
-          s_c[i] = g.aux[2 * plane + gi];
+        const bool ok = i < nst * 32 && l < cnt && in_range(lay.at(row0 + l, ts + k), plane) &&
+                        in_range(i, SROWS * 32);
+        const int64_t gi = ok ? lay.at(row0 + l, ts + k) : 0;
+        ev[u] = ok ? __ldg(g.aux + gi) : 0.f;
+        qa[u] = ok ? __ldg(g.aux + plane + gi) : 0.f;
+        cc[u] = ok ? __ldg(g.aux + 2 * plane + gi) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int i = threadIdx.x + u * BLOCK;
+        if (i < nst * 32 && i < SROWS * 32) {
+          s_ev[i] = ev[u];
+          s_qa[i] = qa[u];
+          s_c[i] = cc[u];
         }
       }
       __syncthreads();

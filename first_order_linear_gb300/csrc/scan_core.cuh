@@ -110,8 +110,14 @@ struct Stor<bf16> {
     o[0] = __uint_as_float(w.x << 16), o[1] = __uint_as_float(w.x & 0xffff0000u);
     o[2] = __uint_as_float(w.y << 16), o[3] = __uint_as_float(w.y & 0xffff0000u);
   }
+  // two elements rounded to nearest even in one conversion, the first in
+  // the low half (the element at the lower address)
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
   __device__ __forceinline__ static void st4(float* p, int64_t i, const float* v) {
-    const uint2 w = make_uint2(to_bits(v[0]) | (to_bits(v[1]) << 16), to_bits(v[2]) | (to_bits(v[3]) << 16));
+    const uint2 w = make_uint2(pack2(v[0], v[1]), pack2(v[2], v[3]));
     *reinterpret_cast<uint2*>(reinterpret_cast<unsigned short*>(p) + i) = w;
   }
   // eight consecutive elements starting at a 16-byte boundary (zeros where !ok)
@@ -124,8 +130,7 @@ struct Stor<bf16> {
     o[6] = __uint_as_float(w.w << 16), o[7] = __uint_as_float(w.w & 0xffff0000u);
   }
   __device__ __forceinline__ static void st8(float* p, int64_t i, const float* v) {
-    const uint4 w = make_uint4(to_bits(v[0]) | (to_bits(v[1]) << 16), to_bits(v[2]) | (to_bits(v[3]) << 16),
-                               to_bits(v[4]) | (to_bits(v[5]) << 16), to_bits(v[6]) | (to_bits(v[7]) << 16));
+    const uint4 w = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
     *reinterpret_cast<uint4*>(reinterpret_cast<unsigned short*>(p) + i) = w;
   }
 };

@@ -537,3 +537,42 @@ def test_time_major_tile_copies_leave_status_clean(cuda_lib, kind, E, T):
     parity.check_case(kind, E, T, seed=E + T, time_major=True)
     assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
     assert st.value == 0, f"device status {st.value:#x}"
+
+
+@pytest.mark.parametrize("kind", ["gae", "vt", "vtrace", "td", "disc", "elig", "psum_i32", "affine_fwd"])
+@pytest.mark.parametrize("E,T", [(8, 64), (1000, 520), (4096, 2048), (256, 4096)])
+def test_time_major_few_envs_repeated_calls(cuda_lib, kind, E, T):
+    """Time-major calls with few environments and rows of several tiles (the
+    direct 8-environment driver, walking tiles; the two-pass split where the
+    rows are long and few), two calls in a row, the second's workspace
+    memory reused from the first: both match the oracle, with the device
+    status word clean."""
+    st = C.c_uint(0)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    for call in range(2):
+        d = parity.make_inputs(kind, E, T, seed=call * 1000 + E + T, trunc=True, device="cuda")
+        parity.check_case(kind, E, T, inputs=d, time_major=True)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    assert st.value == 0, f"device status {st.value:#x}"
+
+
+def test_time_major_bf16_few_envs_workspace_garbage(cuda_lib):
+    """bfloat16 storage, time-major with few environments and long rows (16
+    environments a CTA), with a caller workspace full of 0xFF bytes before
+    each of two calls."""
+    E, T = 1024, 2048
+    need = rlca.rlca_workspace_size(_lib.RLCA_EST_VALUE_TARGETS, E, T, 0, _lib.RLCA_TIME_MAJOR | _lib.RLCA_BF16)
+    ws = torch.full((max(need, 16),), 0xFF, dtype=torch.uint8, device="cuda")
+    for call in range(2):
+        d = parity.to_bf16(parity.make_inputs("vt", E, T, seed=77 + call, trunc=True, device="cuda"))
+        ws.fill_(0xFF)
+        x = parity._tm(d, True)
+        out = rlca.rlca_value_targets(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
+                                      x["bootstrap"], gamma=parity.GAMMA, lambda_=parity.LAMBDA, time_major=True,
+                                      workspace=ws if need > 0 else None)
+        torch.cuda.synchronize()
+        rows = parity.sample_rows(E, T, seed=call)
+        want = parity.run_oracle("vt", d, rows)
+        for o, w, name in zip(out[:3], want[:3], ("adv", "ret", "disc")):
+            parity.assert_close(parity._np(parity._back(o, True), rows), w, f"bf16 time-major {name} call {call}",
+                                tol=parity.BF16_TOL, rel=parity.BF16_REL)
