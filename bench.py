@@ -212,6 +212,73 @@ def cpu_baseline(d, budget_s=6.0):
                                       "sample": f"{repsn} batches of the first {nrows} envs, {eln:.1f} s"}}
 
 
+ORACLE_CONFIGS = [("gae 8x16", 8, 16), ("gae+disc+td 4096x128", 4096, 128), ("vtrace 4096x256", 4096, 256),
+                  ("retrace 1024x2048", 1024, 2048)]
+
+
+def run_oracle_configs(args):
+    """The C oracle on each named configuration, one host thread and all of
+    them (rows split across threads): env-steps per second per estimator,
+    one JSON line per configuration.  Timed for about --oracle-seconds each."""
+    import numpy as np
+    from first_order_linear_gb300 import synth
+    cores = _host_cores()
+    budget = args.oracle_seconds
+    for name, E_, T_ in ORACLE_CONFIGS:
+        seed = synth.config_seed(name)
+        if name.startswith("gae"):
+            d = synth.value_rollout(E_, T_, seed, p_term=0.05 if E_ == 8 else P_TERM,
+                                    p_trunc=0.02 if E_ == 8 else P_TRUNC, with_trunc=True)
+            fns = ["gae"] if E_ == 8 else ["gae", "discounted_return", "td_lambda"]
+        elif name.startswith("vtrace"):
+            d = synth.vtrace_rollout(E_, T_, seed, p_term=0.01)
+            fns = ["vtrace"]
+        else:
+            d = synth.retrace_rollout(E_, T_, seed, p_term=0.002)
+            fns = ["retrace"]
+        n = _oracle_inputs(d, E_)
+
+        def one(x, fns=fns):
+            from oracle import ref_c
+            for f in fns:
+                if f == "gae":
+                    ref_c.gae(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
+                              x["bootstrap"], gamma=GAMMA, lam=LAMBDA)
+                elif f == "discounted_return":
+                    ref_c.discounted_return(x["rewards"], x["terminated"], x["truncated"], x["trunc_value"],
+                                            x["bootstrap"], gamma=GAMMA)
+                elif f == "td_lambda":
+                    ref_c.td_lambda(x["rewards"], x["values"], x["terminated"], x["truncated"], x["trunc_value"],
+                                    x["bootstrap"], gamma=GAMMA, lam=LAMBDA)
+                elif f == "vtrace":
+                    ref_c.vtrace(x["rewards"], x["values"], x["logp_target"], x["logp_behaviour"],
+                                 x["terminated"], x.get("truncated"), x.get("trunc_value"), x["bootstrap"],
+                                 gamma=GAMMA)
+                else:
+                    ref_c.retrace(x["q"], x["pi"], x["mu_a"], x["actions"], x["rewards"], x["terminated"],
+                                  x.get("truncated"), x.get("trunc_value"), x["bootstrap"], gamma=GAMMA,
+                                  lam=LAMBDA)
+        line = {"oracle_config": name, "E": E_, "T": T_, "estimators": fns, "unit": "env-steps/s per estimator"}
+        for threads in (1, cores):
+            pool = None
+            if threads > 1:
+                import concurrent.futures as cf
+                pool = cf.ThreadPoolExecutor(max_workers=threads)
+                parts = _row_slices(n, threads)
+
+                def step(x, pool=pool, parts=parts):
+                    for f in [pool.submit(one, p) for p in parts]:
+                        f.result()
+            else:
+                step = one
+            reps, el = _time_oracle(step, n, budget)
+            if pool is not None:
+                pool.shutdown()
+            line[f"threads_{threads}"] = {"value": E_ * T_ * reps / el, "reps": reps, "seconds": round(el, 2)}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -1211,6 +1278,9 @@ def main():
     ap.add_argument("--skip-torch-compile", action="store_true", help="with --torch-baseline: eager only")
     ap.add_argument("--pages-protocol", action="store_true",
                     help="time the named configurations with the paper's protocol (cold L2, isolated calls)")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="time the C oracle on each named configuration, one thread and all host cores")
+    ap.add_argument("--oracle-seconds", type=float, default=3.0)
     ap.add_argument("--pages-flush", choices=["read", "write"], default="read",
                     help="with --pages-protocol: flush L2 by reading (default) or by a memset of 2 x L2")
     ap.add_argument("--ncu-case", default="",
@@ -1226,6 +1296,8 @@ def main():
         return run_torch_baseline(args)
     if args.pages_protocol:
         return run_pages_protocol(args)
+    if args.oracle_configs:
+        return run_oracle_configs(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -214,8 +214,14 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     // bytes a step: it splits only when the rows are 8x fewer still)
     const int64_t threads = q.row_blocks * q.block;
     const int64_t target = (int64_t)sm_count * 1024;
-    if (q.ntiles > 1 && 2 * threads < target && (!retrace || 16 * threads < target))
+    if (q.ntiles > 1 && 2 * threads < target && (!retrace || 16 * threads < target)) {
       nseg = (int)std::min<int64_t>(q.ntiles, (target + threads - 1) / threads);
+      // Retrace CTAs are held to a few an SM by their staging buffers:
+      // split to that many CTAs rather than to a thread count
+      if (retrace && kRetraceSplitCtasPerSm > 0)
+        nseg = (int)std::min<int64_t>(
+            q.ntiles, ((int64_t)kRetraceSplitCtasPerSm * sm_count + q.row_blocks - 1) / q.row_blocks);
+    }
   }
   const int seg_tiles = (q.ntiles + nseg - 1) / nseg;
   q.seg_len = seg_tiles * q.tile;
@@ -245,7 +251,9 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   const int W8 = next_pow2((T + 7) / 8);
   const int64_t l8_min_threads = (int64_t)sm_count * 1024 * (retrace ? 4 : 1);
   const int l8_min_t = (bf16_io && kind != Kind::Vtrace) ? 64 : kFastL8MinT;
-  const bool l8 = (T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads) ||
+  // (float32 V-Trace stays at 4 steps: at 8 it holds 67-80 registers, and
+  // 4 measured faster at T = 2048, 0.78 against 0.75 of the bandwidth)
+  const bool l8 = ((kind != Kind::Vtrace || bf16_io) && T >= l8_min_t && (int64_t)E * (T / 8) >= l8_min_threads) ||
                   (!bf16_io && kind != Kind::Vtrace && T >= 256 && (int64_t)E * (T / 8) >= 2 * l8_min_threads);
   if (fast_ok && l8 && T % 8 == 0 && W8 <= (retrace ? kRetraceEmMaxWidth : kEmMaxWidth)) {
     q.fast = true;

@@ -420,7 +420,9 @@ struct VtraceEst : NoStage {
     load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
 #pragma unroll
     for (int k = 0; k < L; ++k) {
-      const float ratio = expf(a[k] - bb[k]);
+      // the hardware exponential: a relative error of a few ulp, far inside
+      // the 1e-4 tolerance, at a fraction of the accurate expf's instructions
+      const float ratio = __expf(a[k] - bb[k]);
       R.rho[k] = fminf(rho_bar, ratio);
       R.c[k] = lambda * fminf(c_bar, ratio);
     }

@@ -115,6 +115,14 @@ constexpr int kTbCtasPerSm = RLCA_TB_CTAS_PER_SM;
 #endif
 // environments per SM from which time-major calls take the bulk driver
 constexpr int kTbMinEnvsPerSm = RLCA_TB_MIN_ENVS_PER_SM;
+#ifndef RLCA_RETRACE_SPLIT_CTAS_PER_SM
+#define RLCA_RETRACE_SPLIT_CTAS_PER_SM 2
+#endif
+// Retrace's two-pass split: CTAs per SM to split rows into (0: by threads).
+// Its staging buffers hold it to two CTAs an SM; splitting to that (rather
+// than to a thread count) measured 0.55 against 0.50 of the bandwidth at
+// 1024 x 2048 time-major, the same elsewhere
+constexpr int kRetraceSplitCtasPerSm = RLCA_RETRACE_SPLIT_CTAS_PER_SM;
 
 // Launches the scan of one estimator functor (both passes of the two-pass
 // path when p.nseg > 1).  Defined by explicit instantiation in the family
