@@ -290,25 +290,28 @@ __device__ __forceinline__ void em_fast_scan(const Est& est, typename Est::templ
 #ifndef RLCA_EM_CAP_VTRACE
 #define RLCA_EM_CAP_VTRACE 0
 #endif
+// threads an SM the driver is compiled to keep resident at 4 steps a
+// thread (0: the compiler's choice)
 template <class Est>
 struct EmRegCap {
-  static constexpr bool value = true;
+  static constexpr int threads = 2048;
 };
 template <bool H, class ST>
 struct EmRegCap<RetraceEst<H, ST>> {
-  static constexpr bool value = false;
+  static constexpr int threads = 0;
 };
 template <class ST>
 struct EmRegCap<VtraceEst<true, ST>> {
-  static constexpr bool value = false;
+  static constexpr int threads = 0;
 };
 template <class ST>
 struct EmRegCap<VtraceEst<false, ST>> {
-  static constexpr bool value = RLCA_EM_CAP_VTRACE != 0;
+  static constexpr int threads = RLCA_EM_CAP_VTRACE == 1 ? 2048 : (RLCA_EM_CAP_VTRACE == 2 ? 1536 : 0);
 };
 template <class Est, int BLOCK, int LS>
 __host__ __device__ constexpr int em_fast_min_blocks() {
-  return (EmRegCap<Est>::value && LS == 4) ? 2048 / BLOCK : 1;
+  return (EmRegCap<Est>::threads > 0 && LS == 4 && EmRegCap<Est>::threads >= BLOCK) ? EmRegCap<Est>::threads / BLOCK
+                                                                                     : 1;
 }
 
 template <class Est, int TPR, int LS>
