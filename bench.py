@@ -748,41 +748,54 @@ def run_e2e(args, d_cpu, dev):
     for k, v in views(host_block).items():
         if v is not None:
             v.copy_(d_cpu[k])
-    NB = 2
+    NB = args.e2e_buffers
+    LANES = args.e2e_lanes
     dev_blocks = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(NB)]
     devb = [views(blk) for blk in dev_blocks]
     outs = [torch.empty(3, E, T, device=dev) for _ in range(NB)]
     back = [torch.empty(3, E, T, pin_memory=True) for _ in range(NB)]
+
+    def pieces(n):
+        """LANES contiguous [lo, hi) ranges of n elements (each copy engine one)."""
+        cuts = [n * i // LANES for i in range(LANES + 1)]
+        return list(zip(cuts[:-1], cuts[1:]))
+    in_pieces = pieces(size)
+    out_pieces = pieces(back[0].numel())
     h2d = sum(d_cpu[k].numel() * d_cpu[k].element_size() for k in names)
     d2h = back[0].numel() * back[0].element_size()
     STEPS_PER_GRAPH = 20
     P = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
     s_main = torch.cuda.Stream(dev)
-    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    s_ins = [torch.cuda.Stream(dev) for _ in range(LANES)]
+    s_outs = [torch.cuda.Stream(dev) for _ in range(LANES)]
+    s_run = torch.cuda.Stream(dev)
 
     def capture(call):
         """One graph of STEPS_PER_GRAPH pipelined steps (fork from the
         capture stream onto the three pipeline streams, join at the end)."""
-        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_in = [[torch.cuda.Event() for _ in range(LANES)] for _ in range(NB)]
         ev_run = [torch.cuda.Event() for _ in range(NB)]
-        ev_out = [torch.cuda.Event() for _ in range(NB)]
+        ev_out = [[torch.cuda.Event() for _ in range(LANES)] for _ in range(NB)]
         started = [False] * NB
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s_main):
-            for st in (s_in, s_run, s_out):
+            for st in s_ins + s_outs + [s_run]:
                 st.wait_stream(s_main)
             for i in range(STEPS_PER_GRAPH):
                 j = i % NB
                 x, o = devb[j], outs[j]
-                with torch.cuda.stream(s_in):
-                    if started[j]:
-                        s_in.wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
-                    dev_blocks[j].copy_(host_block, non_blocking=True)
-                    ev_in[j].record(s_in)
+                for lane, (lo, hi) in enumerate(in_pieces):  # the copy in, one piece per copy stream
+                    with torch.cuda.stream(s_ins[lane]):
+                        if started[j]:
+                            s_ins[lane].wait_event(ev_run[j])  # this buffer set's previous call has read its inputs
+                        dev_blocks[j][lo:hi].copy_(host_block[lo:hi], non_blocking=True)
+                        ev_in[j][lane].record(s_ins[lane])
                 with torch.cuda.stream(s_run):
-                    s_run.wait_event(ev_in[j])
+                    for e in ev_in[j]:
+                        s_run.wait_event(e)
                     if started[j]:
-                        s_run.wait_event(ev_out[j])  # its previous outputs have left
+                        for e in ev_out[j]:
+                            s_run.wait_event(e)  # its previous outputs have left
                     if call:
                         st = lib.rlca_value_targets(
                             P(x["rewards"]), P(x["values"]), P(x["terminated"]), P(x["truncated"]),
@@ -791,12 +804,13 @@ def run_e2e(args, d_cpu, dev):
                         if st != 0:
                             raise RuntimeError(f"rlca_value_targets failed with status {st}")
                     ev_run[j].record(s_run)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_run[j])
-                    back[j].copy_(o, non_blocking=True)
-                    ev_out[j].record(s_out)
+                for lane, (lo, hi) in enumerate(out_pieces):  # the copy out, likewise
+                    with torch.cuda.stream(s_outs[lane]):
+                        s_outs[lane].wait_event(ev_run[j])
+                        back[j].view(-1)[lo:hi].copy_(o.view(-1)[lo:hi], non_blocking=True)
+                        ev_out[j][lane].record(s_outs[lane])
                 started[j] = True
-            for st in (s_in, s_run, s_out):
+            for st in s_ins + s_outs + [s_run]:
                 s_main.wait_stream(st)
         _upload(g, s_main)
         return g
@@ -834,8 +848,9 @@ def run_e2e(args, d_cpu, dev):
                                   "GBps_in_plus_out": (h2d + d2h) * steps / (ms_link / 1e3) / 1e9,
                                   "how": "the same pipelined pinned copies in and out, without the call"},
             "frac_of_host_link_ceiling": ms_link / ms,
-            "pipeline": f"per step one packed pinned-host copy in, the C-ABI call, one packed copy out, on three "
-                        f"streams over two device buffer sets; {STEPS_PER_GRAPH} steps per CUDA graph, replayed"}
+            "pipeline": f"per step the packed pinned-host inputs copied in as {LANES} pieces on {LANES} streams, "
+                        f"the C-ABI call on its own stream, the packed outputs copied out as {LANES} pieces on {LANES} "
+                        f"more, over {NB} device buffer sets; {STEPS_PER_GRAPH} steps per CUDA graph, replayed"}
 
 
 # --------------------------------------------------------------------------
@@ -1266,6 +1281,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e pipeline")
+    ap.add_argument("--e2e-buffers", type=int, default=2, help="device buffer sets of the e2e pipeline")
     ap.add_argument("--sweep", action="store_true",
                     help="print one line per estimator and benchmark shape instead of the step metric")
     ap.add_argument("--sweep-kinds", default="", help="comma-separated subset of " + ",".join(SWEEP_KINDS))
