@@ -351,6 +351,31 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
   return true;
 }
 
+bool retrace_tail_plan(const Plan& p, int64_t E, int T, bool two_byte, Plan* out) {
+  if (!p.time_major || p.nseg < 2 || T % 8 != 0 || (uint64_t)E * (uint64_t)T >= (uint64_t{1} << 32)) return false;
+  const int EW = two_byte ? 16 : 8;  // one 32-byte sector of a step row
+  int CT = 32;
+  while (CT > 1 && p.seg_len % (8 * CT) != 0) CT /= 2;
+  if (EW * CT < 32 || p.seg_len % (8 * CT) != 0) return false;  // whole warps
+  Plan q = p;
+  q.fast = false;
+  q.tm_fast = true;
+  q.tm_staged = false;
+  q.tm_bulk = false;
+  q.env_width = EW;
+  q.width = CT;
+  q.block = EW * CT;
+  q.rows_per_cta = EW;
+  q.tile = 8 * CT;
+  q.ntiles = (T + q.tile - 1) / q.tile;
+  q.row_blocks = (E + EW - 1) / EW;
+  q.smem = 0;
+  q.smem_driver_bound = (size_t)CT * (EW + 1) * (kMaxMapBytes + kMaxMapBytes / 2);
+  if (q.row_blocks * q.nseg > INT32_MAX) return false;
+  *out = q;
+  return true;
+}
+
 StageCounts stage_counts(Kind kind) {
   switch (kind) {
     case Kind::Gae:

@@ -258,6 +258,45 @@ static cudaError_t launch_pass(const Plan& p, const Est& est, const Geom& g, cud
   }
 }
 
+// Retrace's second pass on the fast time-major driver where the plan
+// allows it (retrace_tail_plan); false: not taken, the caller runs the
+// first pass's kernel again
+template <class Est>
+static bool launch_retrace_tail(const Est&, const Plan&, const Geom&, cudaStream_t, cudaError_t*) {
+  return false;
+}
+template <bool H, class ST>
+static bool launch_retrace_tail(const RetraceEst<H, ST>& est, const Plan& p, const Geom& g, cudaStream_t s,
+                                cudaError_t* err) {
+  Plan q;
+  if (g.aux == nullptr || !retrace_tail_plan(p, g.E, g.T, sizeof(ST) == 2, &q)) return false;
+  RetraceTailEst<H, ST> tail;
+  tail.b = est.b;
+  tail.r = est.r;
+  tail.aux = g.aux;
+  tail.plane = g.E * (int64_t)g.T;
+  tail.out = est.out;
+  tail.gamma = est.gamma;
+  if constexpr (sizeof(ST) == 2) {
+    switch (q.width) {
+      case 2: *err = launch_tf<RetraceTailEst<H, ST>, 16, 2>(q, tail, g, s); return true;
+      case 4: *err = launch_tf<RetraceTailEst<H, ST>, 16, 4>(q, tail, g, s); return true;
+      case 8: *err = launch_tf<RetraceTailEst<H, ST>, 16, 8>(q, tail, g, s); return true;
+      case 16: *err = launch_tf<RetraceTailEst<H, ST>, 16, 16>(q, tail, g, s); return true;
+      case 32: *err = launch_tf<RetraceTailEst<H, ST>, 16, 32>(q, tail, g, s); return true;
+      default: return false;
+    }
+  } else {
+    switch (q.width) {
+      case 4: *err = launch_tf<RetraceTailEst<H, ST>, 8, 4>(q, tail, g, s); return true;
+      case 8: *err = launch_tf<RetraceTailEst<H, ST>, 8, 8>(q, tail, g, s); return true;
+      case 16: *err = launch_tf<RetraceTailEst<H, ST>, 8, 16>(q, tail, g, s); return true;
+      case 32: *err = launch_tf<RetraceTailEst<H, ST>, 8, 32>(q, tail, g, s); return true;
+      default: return false;
+    }
+  }
+}
+
 template <class Est>
 cudaError_t run_scan(const Est& est, const Plan& p, const Geom& g0, cudaStream_t s) {
   TmaSet maps;  // filled for the bulk driver only (the other drivers never read it)
@@ -275,6 +314,8 @@ cudaError_t run_scan(const Est& est, const Plan& p, const Geom& g0, cudaStream_t
     g.mode = kModeAggregate;
     cudaError_t e = launch_pass(p, est, g, s, maps);
     if (e != cudaSuccess) return e;
+    g.mode = kModeFull;
+    if (launch_retrace_tail(est, p, g, s, &e)) return e;
   }
   g.mode = kModeFull;
   return launch_pass(p, est, g, s, maps);

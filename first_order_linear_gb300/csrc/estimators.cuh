@@ -844,6 +844,91 @@ struct RetraceEst {
   }
 };
 
+// Second pass of Retrace's two-pass split.  The first pass left every
+// step's (EV, Qa, c) in three float planes of the workspace (element order
+// of the inputs), so this pass is a scan of scalars: r, the flags and the
+// successor step's three plane values build the same (alpha_t, beta_t) as
+// RetraceEst::coef, without the per-action blocks or shared-memory staging.
+// It runs on the fast time-major driver, whose CTAs of 8 (16 for bfloat16)
+// environments give the few-environment, long-row problems that take the
+// split several times the CTAs of the first pass.
+template <bool HAS_TRUNC, class ST = float>
+struct RetraceTailEst : NoStage {
+  using Store = ST;
+  using V = float;
+  static constexpr bool kBackward = true;
+  static constexpr int kNb = 3;  // the next chunk's first (EV, Qa, c)
+  static constexpr bool kStageable = false;
+  static constexpr int kSF = 0, kSB = 0;
+  BoundaryArgs b;
+  const float* r;
+  const float* aux;  // planes EV, Qa, c of E * T floats each
+  int64_t plane;     // E * T
+  float* out;
+  float gamma;
+
+  template <int L>
+  struct Regs {
+    BoundaryRegs<L> bd;
+    float r[L], ev[L], qa[L], c[L], o[L];
+    float evn, qan, cn;  // step t0 + L
+  };
+  __device__ __forceinline__ float row_carry(int64_t) const { return 0.f; }
+
+  template <int L, class IO>
+  __device__ __forceinline__ void load(Regs<L>& R, const IO& io, int, int, int, int, unsigned char*) const {
+    io.template f<L>(0, r, R.r);
+    load_boundary<HAS_TRUNC, ST, L>(b, R.bd, io);
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const int64_t i = io.at(k);
+      const bool ok = k < io.n && in_range(i, plane);
+      R.ev[k] = ok ? __ldg(aux + i) : 0.f;
+      R.qa[k] = ok ? __ldg(aux + plane + i) : 0.f;
+      R.c[k] = ok ? __ldg(aux + 2 * plane + i) : 0.f;
+    }
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_give(const Regs<L>& R, float* g) const {
+    g[0] = R.ev[0];
+    g[1] = R.qa[0];
+    g[2] = R.c[0];
+  }
+  template <class Lay>
+  __device__ __forceinline__ void nb_load(const Lay& lay, int64_t row, int t, float* g) const {
+    const int64_t i = lay.at(row, t);
+    g[0] = __ldg(aux + i);
+    g[1] = __ldg(aux + plane + i);
+    g[2] = __ldg(aux + 2 * plane + i);
+  }
+  template <int L>
+  __device__ __forceinline__ void nb_take(Regs<L>& R, const float* g) const {
+    R.evn = g[0];
+    R.qan = g[1];
+    R.cn = g[2];
+  }
+  template <int L>
+  __device__ __forceinline__ Aff<float> coef(const Regs<L>& R, int k, int t) const {
+    const float evs = k + 1 < L ? R.ev[k + 1] : R.evn;
+    const float qas = k + 1 < L ? R.qa[k + 1] : R.qan;
+    const float cs = k + 1 < L ? R.c[k + 1] : R.cn;
+    const bool tm = (R.bd.term >> k) & 1u, tr = (R.bd.trunc >> k) & 1u;
+    const bool last = t == b.T - 1;
+    const float interior = evs - cs * qas;
+    const float tail = tm ? 0.f : (tr ? R.bd.tv[k] : (last ? R.bd.boot : interior));
+    const float beta = (tm || tr || last) ? 0.f : gamma * cs;
+    return {R.r[k] + gamma * tail, beta};
+  }
+  template <int L>
+  __device__ __forceinline__ void emit(Regs<L>& R, int k, float A, float, const Aff<float>&) const {
+    R.o[k] = A;
+  }
+  template <int L, class IO>
+  __device__ __forceinline__ void store(const Regs<L>& R, const IO& io) const {
+    io.template put<L>(0, out, R.o);
+  }
+};
+
 // ===========================================================================
 // Eligibility trace, forward (rl-triton §1, §5)
 //   alpha_t = x_t,  beta_t = gamma lambda (1 - d_{t-1}),  e_{-1} = 0

@@ -54,6 +54,15 @@ constexpr size_t aux_offset(size_t ws_bytes, size_t aux_bytes) { return ws_bytes
 bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int sm_count, bool vec, Plan* p,
                bool bulk = false);
 
+// The second pass of Retrace's time-major two-pass split on the fast
+// time-major driver (RetraceTailEst): the first pass's segments (nseg,
+// seg_len) in CTAs of 8 environments (16 for 2-byte storage) and CT chunk
+// threads, CT the largest power of two up to 32 whose 8 * CT steps divide a
+// segment.  False where that driver does not apply (env-major, one
+// segment, T % 8 != 0, E * T >= 2^32); the first pass's kernel then runs
+// the second as well.
+bool retrace_tail_plan(const Plan& p, int64_t E, int T, bool two_byte, Plan* out);
+
 // bytes a time-major step stages per staged input set (float inputs of
 // fbytes each, flag inputs of one byte)
 struct StageCounts {

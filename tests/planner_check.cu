@@ -10,6 +10,8 @@
 //   - CTAs are whole warps and fit the shared-memory limit;
 //   - the workspace holds one affine map per (row, segment) when rows are
 //     split, Retrace's per-step scalar planes after them, nothing otherwise;
+//   - Retrace's time-major second pass (retrace_tail_plan) keeps the first
+//     pass's segments in whole tiles of a fast time-major kernel that exists;
 //   - tensor-copy tiles: each stage buffer starts on a 128-byte boundary,
 //     the largest stage index a thread reads is the buffer's last element,
 //     a box is at most 256 rows of whole 16-byte rows, the kernel's shared
@@ -65,7 +67,7 @@ int main() {
   const long Es[] = {1, 3, 8, 33, 256, 1000, 1024, 4096, 9728, 9744, 16384, 65536};
   const int Ts[] = {1, 7, 8, 16, 31, 64, 128, 129, 256, 512, 520, 2048, 4096, 40000, 140001};
   const int sms = 152;
-  long checked = 0, n_fast = 0, n_tm_fast = 0, n_staged = 0, n_bulk = 0, n_split = 0;
+  long checked = 0, n_fast = 0, n_tm_fast = 0, n_staged = 0, n_bulk = 0, n_split = 0, n_tail = 0;
   for (int ki = 0; ki < 9; ++ki) {
     const Kind kind = kinds[ki];
     for (long E : Es)
@@ -118,6 +120,23 @@ int main() {
               } else if (p.ws_bytes != 0) {
                 fail("workspace without a split", ki, E, T, flags, p);
               }
+              if (kind == Kind::Retrace) {
+                Plan q;
+                const bool b16 = (flags & RLCA_BF16) != 0;
+                if (retrace_tail_plan(p, E, T, b16, &q)) {
+                  ++n_tail;
+                  const int EW = b16 ? 16 : 8;
+                  const bool widths = b16 ? (q.width >= 2 && q.width <= 32) : (q.width >= 4 && q.width <= 32);
+                  if (!tm || p.nseg < 2 || T % 8 != 0 || (unsigned long long)E * T >= (1ull << 32) ||
+                      q.env_width != EW || !widths || (q.width & (q.width - 1)) != 0 || q.block != EW * q.width ||
+                      q.block % 32 != 0 || q.tile != 8 * q.width || q.seg_len != p.seg_len || q.nseg != p.nseg ||
+                      q.seg_len % q.tile != 0 || (long long)q.row_blocks * EW < E || !q.tm_fast || q.tm_staged ||
+                      q.tm_bulk || q.smem + q.smem_driver_bound > kMaxSmemPerCta)
+                    fail("Retrace second pass", ki, E, T, flags, q);
+                } else if (tm && p.nseg > 1 && T % 8 == 0 && (unsigned long long)E * T < (1ull << 32)) {
+                  fail("Retrace second pass not taken", ki, E, T, flags, p);
+                }
+              }
               if (p.tm_bulk) {
                 const bool b16 = (flags & RLCA_BF16) != 0;
                 bool ok = bulk && tm && E % 16 == 0 && T % 8 == 0 && E >= 64L * sms;
@@ -140,7 +159,7 @@ int main() {
     std::printf("planner: %d failures in %ld plans\n", g_bad, checked);
     return 1;
   }
-  std::printf("planner ok %ld fast %ld tm_fast %ld staged %ld bulk %ld two_pass %ld\n", checked, n_fast, n_tm_fast,
-              n_staged, n_bulk, n_split);
+  std::printf("planner ok %ld fast %ld tm_fast %ld staged %ld bulk %ld two_pass %ld retrace_tail %ld\n", checked,
+              n_fast, n_tm_fast, n_staged, n_bulk, n_split, n_tail);
   return 0;
 }

@@ -237,6 +237,19 @@ def test_retrace_time_major_widths():
             parity.check_case("retrace", E, T, seed=70 + i, time_major=True, num_actions=A, bf16=bf16)
 
 
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("E,T", [(13, 2048), (256, 2048), (1000, 1000), (1001, 1003), (40, 4096), (8, 72)])
+def test_retrace_time_major_second_pass(E, T, bf16):
+    """Time-major Retrace on few environments splits rows into segments; the
+    second pass scans the per-step scalars the first left in the workspace
+    on the fast time-major driver (CTAs of 8 environments, 16 for bfloat16,
+    1 to 32 chunk threads to fit the segment) when T % 8 == 0, and with the
+    first pass's kernel otherwise (T = 1003).  Ragged E, truncation on, also
+    with termination everywhere in some rows."""
+    parity.check_case("retrace", E, T, seed=E + T, time_major=True, bf16=bf16, p_term=0.002)
+    parity.check_case("retrace", E, T, seed=E + T + 1, time_major=True, bf16=bf16, p_term=0.3)
+
+
 def test_vtrace_clipping_and_lambda():
     p = dict(rho_bar=1.3, c_bar=0.7, vt_lambda=0.9)
     for tm in (False, True):

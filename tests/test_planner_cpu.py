@@ -34,7 +34,8 @@ def harness(tmp_path_factory):
 def test_planner_invariants(harness):
     out = subprocess.run([harness], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stdout[-3000:]
-    m = re.search(r"planner ok (\d+) fast (\d+) tm_fast (\d+) staged (\d+) bulk (\d+) two_pass (\d+)", out.stdout)
+    m = re.search(r"planner ok (\d+) fast (\d+) tm_fast (\d+) staged (\d+) bulk (\d+) two_pass (\d+) "
+                  r"retrace_tail (\d+)", out.stdout)
     assert m, out.stdout
     total, *per_driver = (int(x) for x in m.groups())
     assert total > 20000
