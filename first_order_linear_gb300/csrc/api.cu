@@ -293,18 +293,28 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     int EW = staged16 ? 16 : tf_ew;
     int CT = staged32 ? std::min(tf_ct, 8) : tf_ct;
     // bulk: each tile of each input is one tensor copy into a ring of
-    // RLCA_TB_STAGES stages, 32 environments per CTA, once E gives two such
-    // CTAs per SM; chunk-threads so the ring stays within kTbRingBytes and a
-    // CTA within 256 threads.  (With fewer environments, 16-environment
-    // CTAs -- the narrowest whose flag rows are 16 bytes -- measured slower
-    // than the direct 8-environment driver, split into two passes or not.)
+    // RLCA_TB_STAGES stages, 32 environments per CTA once E gives two such
+    // CTAs per SM, else 8 (below); chunk-threads so the ring stays within
+    // kTbRingBytes and a CTA within 256 threads.  (16-environment CTAs,
+    // split into two passes or not, measured slower than the direct
+    // 8-environment driver.)
     const StageCounts sc = stage_counts(kind);
-    const size_t step_bytes = (size_t)sc.nf * (bf16_io ? 2 : 4) + (size_t)sc.nb;
-    if (kTmBulk && bulk && E % 16 == 0 && E >= (int64_t)kTbMinEnvsPerSm * sm_count) {
-      EW = 32;
+    const bool wide = E >= (int64_t)kTbMinEnvsPerSm * sm_count;
+    // 8-environment tiles (one 32-byte sector of a float32 step row, the
+    // flag rows copied 16 environments wide) where they pay: two or more
+    // float inputs, rows of several 256-step tiles, and enough CTAs of 8
+    // environments that rows stay whole (one pass).  Measured against the
+    // direct driver at 4096 x 2048: 1.08-1.13x; at 4096 x 128-512, with
+    // one float input, or split into two passes: 0.65-1.0x.
+    const int narrow_ct = std::max(4, std::min(ct_need, 32));
+    const bool narrow = kTbNarrow && !bf16_io && sc.nf >= 2 && (E / 8) >= (int64_t)kTbCtasPerSm * sm_count &&
+                        (T + 8 * narrow_ct - 1) / (8 * narrow_ct) >= kTbNarrowMinTiles;
+    if (kTmBulk && bulk && E % 16 == 0 && (wide || narrow)) {
+      EW = wide ? 32 : 8;
+      const size_t row_bytes = (size_t)sc.nf * (bf16_io ? 2 : 4) * EW + (size_t)sc.nb * (EW < 16 ? 16 : EW);
       const int ct_min = 32 / EW;  // whole warps
       CT = std::max(ct_min, std::min(ct_need, 256 / EW));
-      while (CT > ct_min && (size_t)RLCA_TB_STAGES * 8 * CT * EW * step_bytes > kTbRingBytes) CT /= 2;
+      while (CT > ct_min && (size_t)RLCA_TB_STAGES * 8 * CT * row_bytes > kTbRingBytes) CT /= 2;
       staged = false;
       q.tm_bulk = true;
     }
@@ -342,7 +352,9 @@ bool make_plan(Kind kind, int64_t E, int T, int num_actions, uint32_t flags, int
     // the stages: at most 4 float and 2 flag inputs of CT * (8 * EW + EW) elements
     if (staged) q.smem_driver_bound += (size_t)RLCA_TS_STAGES * ((size_t)CT * 9 * EW * 18 + 16);
     // barriers, alignment slack and the tensor-copy ring
-    if (q.tm_bulk) q.smem_driver_bound += 256 + (size_t)RLCA_TB_STAGES * 8 * CT * EW * step_bytes;
+    if (q.tm_bulk)
+      q.smem_driver_bound +=
+          256 + (size_t)RLCA_TB_STAGES * 8 * CT * ((size_t)sc.nf * (bf16_io ? 2 : 4) * EW + (size_t)sc.nb * (EW < 16 ? 16 : EW));
   }
   if (q.row_blocks * q.nseg > INT32_MAX) return false;
   if (q.smem + q.smem_driver_bound > kMaxSmemPerCta) return false;
@@ -436,7 +448,7 @@ bool encode_tm_maps(const StagedList& in, int elem_bytes, int64_t E, int64_t T, 
   for (int i = 0; i < in.nf; ++i)
     if (!encode_2d(&out->f[i], in.fin[i], elem_bytes, E, T, ew, rows)) return false;
   for (int i = 0; i < in.nb; ++i)
-    if (in.bin[i] != nullptr && !encode_2d(&out->b[i], in.bin[i], 1, E, T, ew, rows)) return false;
+    if (in.bin[i] != nullptr && !encode_2d(&out->b[i], in.bin[i], 1, E, T, ew < 16 ? 16 : ew, rows)) return false;
   return true;
 }
 

@@ -153,6 +153,17 @@ static cudaError_t launch_tb(const Plan& p, const Est& est, const Geom& g, cudaS
 
 template <class Est>
 static cudaError_t launch_tb_any(const Plan& p, const Est& est, const Geom& g, cudaStream_t s, const TmaSet& maps) {
+  if constexpr (sizeof(typename Est::Store) == 4) {
+    if (p.env_width == 8) {
+      switch (p.width) {
+        case 4: return launch_tb<Est, 8, 4>(p, est, g, s, maps);
+        case 8: return launch_tb<Est, 8, 8>(p, est, g, s, maps);
+        case 16: return launch_tb<Est, 8, 16>(p, est, g, s, maps);
+        case 32: return launch_tb<Est, 8, 32>(p, est, g, s, maps);
+        default: return cudaErrorInvalidConfiguration;
+      }
+    }
+  }
   if (p.env_width == 16) {
     switch (p.width) {
       case 2: return launch_tb<Est, 16, 2>(p, est, g, s, maps);

@@ -744,8 +744,8 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
     const int t0 = ts + c * L;
     const int n = (row_ok && t0 < seg_hi) ? L : 0;
     const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
-    const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
-                           (uint32_t)t0 * E32 + (uint32_t)row, E32, E32 * (uint32_t)g.T};
+    const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, c * CS + j, row, t0, n,
+                               (uint32_t)t0 * E32 + (uint32_t)row, E32, E32 * (uint32_t)g.T};
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);
@@ -821,7 +821,10 @@ __global__ void __launch_bounds__(TsShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Ts
 // inputs, one 2-D tensor map per staged input (TmaSet, encoded on the host).
 // Per tile and input, thread 0 issues one cp.async.bulk.tensor copy of the
 // [TILE, EW] block into a ring of NS stages, NS - 1 tiles ahead of the scan;
-// completion is counted in bytes on the stage's mbarrier.  No thread issues
+// completion is counted in bytes on the stage's mbarrier.  A copy's rows
+// are at least 16 bytes wide: CTAs of 8 environments copy the flag rows of
+// the aligned 16 environments that hold theirs and read their half.  No
+// thread issues
 // per-element copies, so the bytes in flight are set by the ring, not by
 // registers or occupancy.  Every wait is bounded (mbar_wait_bounded): a
 // copy that never lands sets the status word and the CTA returns.
@@ -834,13 +837,16 @@ struct TbShape : TfShape<EW, CT> {
   static constexpr int NS = RLCA_TB_STAGES;
   static constexpr int CS = TfShape<EW, CT>::L * EW;  // chunk stride in a stage buffer: [TILE][EW], dense
   static constexpr int FB = CT * CS;                  // elements per staged buffer (= TILE * EW)
-  static_assert(EW == 16 || EW == 32, "16-byte rows of flags: at least 16 environments");
+  static constexpr int FW = EW < 16 ? 16 : EW;        // bytes per staged flag row (16 at least)
+  static constexpr int FBB = TfShape<EW, CT>::TILE * FW;  // bytes per staged flag buffer
+  static_assert(EW == 8 || EW == 16 || EW == 32, "float rows of 32 bytes or more");
 };
 template <class Est, int EW, int CT>
 __host__ __device__ constexpr size_t tb_stage_bytes() {
-  // FB * element size is a multiple of 128 for EW >= 16, so every buffer
-  // starts on a 128-byte boundary
-  return (size_t)TbShape<EW, CT>::FB * (sizeof(typename Est::Store) * Est::kSF + Est::kSB);
+  // FB * element size and FBB are multiples of 128 (TILE % 8 == 0, rows of
+  // >= 16 bytes), so every buffer starts on a 128-byte boundary
+  return (size_t)TbShape<EW, CT>::FB * sizeof(typename Est::Store) * Est::kSF +
+         (size_t)TbShape<EW, CT>::FBB * Est::kSB;
 }
 template <class Est, int EW, int CT>
 __host__ __device__ constexpr size_t tb_smem_bytes() {
@@ -856,7 +862,7 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
   using V = typename Est::V;
   constexpr bool BWD = Est::kBackward;
   using ST = typename Est::Store;
-  constexpr int L = S::L, PAD = S::PAD, NS = S::NS, CS = S::CS, FB = S::FB;
+  constexpr int L = S::L, PAD = S::PAD, NS = S::NS, CS = S::CS, FB = S::FB, FW = S::FW, FBB = S::FBB;
   constexpr int ES = (int)sizeof(ST);
   constexpr size_t STAGE = tb_stage_bytes<Est, EW, CT>();
   constexpr size_t FLAGS_AT = (size_t)ES * Est::kSF * FB;  // flag buffers' offset in a stage
@@ -882,6 +888,9 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
   const uint32_t E32 = (uint32_t)g.E;
   const TimeMajor lay{g.E, g.T};
   const bool early = g.early != 0 && g.nseg == 1;
+  // flag rows: copied from environment fx (16-byte aligned), ours at foff
+  const int fx = EW < 16 ? (int)(row0 & ~int64_t(15)) : (int)row0;
+  const int foff = (int)(row0 - fx);
   pdl_trigger();  // the dependent grid may launch now: it waits for this one before touching our outputs
   if (tid == 0) {
 #pragma unroll
@@ -900,7 +909,7 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
   int nflags = 0;
 #pragma unroll
   for (int b = 0; b < Est::kSB; ++b) nflags += in.bin[b] != nullptr ? 1 : 0;
-  const uint32_t tx_bytes = (uint32_t)(S::TILE * EW) * (uint32_t)(ES * Est::kSF + nflags);
+  const uint32_t tx_bytes = (uint32_t)(S::TILE * EW * ES * Est::kSF) + (uint32_t)(FBB * nflags);
 
   // thread 0: the copies of the it-th tile in processing order into stage it % NS
   auto issue = [&](int it) {
@@ -913,7 +922,7 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
     for (int b = 0; b < Est::kSF; ++b) tma_load_2d(st + (size_t)b * FB * ES, &maps.f[b], (int)row0, ts, bar);
 #pragma unroll
     for (int b = 0; b < Est::kSB; ++b)
-      if (in.bin[b] != nullptr) tma_load_2d(st + FLAGS_AT + (size_t)b * FB, &maps.b[b], (int)row0, ts, bar);
+      if (in.bin[b] != nullptr) tma_load_2d(st + FLAGS_AT + (size_t)b * FBB, &maps.b[b], fx, ts, bar);
   };
   // thread 0, after a wait gave up: let the copies already issued land (each
   // wait bounded again) before the CTA exits
@@ -960,8 +969,9 @@ __global__ void __launch_bounds__(TbShape<EW, CT>::BLOCK, (tf_blocks_for<Est, Tb
     const int n = (row_ok && t0 < seg_hi) ? L : 0;
     const unsigned char* st = ring + (size_t)(it % NS) * STAGE;
     if (!mbar_wait_bounded(&bars[it % NS], (uint32_t)(it / NS) & 1u)) *abort_flag = 1;
-    const TmSIO<EW, FB, ST> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j, row, t0, n,
-                               (uint32_t)t0 * E32 + (uint32_t)row, E32, E32 * (uint32_t)g.T};
+    const TmSIO<EW, FB, ST, FW, FBB> io{reinterpret_cast<const ST*>(st), st + FLAGS_AT, c * CS + j,
+                                        c * L * FW + foff + j, row, t0, n, (uint32_t)t0 * E32 + (uint32_t)row,
+                                        E32, E32 * (uint32_t)g.T};
 
     typename Est::template Regs<L> R;
     est.template load<L>(R, io, 0, ts, S::TILE, EW, nullptr);

@@ -71,8 +71,9 @@ struct StageCounts {
 StageCounts stage_counts(Kind kind);
 
 // The 2-D tensor maps of a call's staged time-major inputs ([T, E], E
-// innermost; tiles of ew environments x rows steps).  False when the
-// encoder is unavailable or refuses a map.
+// innermost; tiles of ew environments x rows steps, flag tiles at least 16
+// environments wide).  False when the encoder is unavailable or refuses a
+// map.
 bool encode_tm_maps(const StagedList& in, int elem_bytes, int64_t E, int64_t T, int ew, int rows, TmaSet* out);
 // whether encode_tm_maps can work at all (the driver's encoder was found)
 bool tensor_maps_available();
@@ -119,6 +120,14 @@ constexpr size_t kTbRingBytes = RLCA_TB_RING_BYTES;
 #endif
 // CTAs per SM below which the bulk driver splits rows into segments
 constexpr int kTbCtasPerSm = RLCA_TB_CTAS_PER_SM;
+#ifndef RLCA_TB_NARROW
+#define RLCA_TB_NARROW 1
+#endif
+// build-time choice: below RLCA_TB_MIN_ENVS_PER_SM environments an SM,
+// float32 time-major tiles of 8 environments move by tensor copies too
+constexpr bool kTbNarrow = RLCA_TB_NARROW != 0;
+// ... for rows of at least this many tiles
+constexpr int kTbNarrowMinTiles = 4;
 #ifndef RLCA_TB_MIN_ENVS_PER_SM
 #define RLCA_TB_MIN_ENVS_PER_SM 64
 #endif

@@ -103,17 +103,19 @@ struct TmIO32 {
   }
 };
 
-// Time-major I/O of the staged time-major driver: inputs from the current
+// Time-major I/O of the staged time-major drivers: inputs from the current
 // shared-memory stage (float input b at fbuf + b * FB elements of type ST,
-// flag input b at bbuf + b * FB; the thread's step k at slot + k * EW),
-// outputs and the rare truncation-value loads straight to global memory as
-// in TmIO32.
-template <int EW, int FB, class ST = float>
+// the thread's step k at slot + k * EW; flag input b at bbuf + b * FBB
+// bytes, step k at fslot + k * FW: flag rows may be staged wider than the
+// CTA's environments), outputs and the rare truncation-value loads straight
+// to global memory as in TmIO32.
+template <int EW, int FB, class ST = float, int FW = EW, int FBB = FB>
 struct TmSIO {
   static constexpr bool kTimeMajor = true;
   const ST* fbuf;
   const uint8_t* bbuf;
   int slot;
+  int fslot;
   int64_t row;
   int t0;
   int n;
@@ -141,10 +143,10 @@ struct TmSIO {
   template <int L>
   __device__ __forceinline__ uint32_t flags(int idx, const uint8_t* p) const {
     if (p == nullptr || n == 0) return 0u;
-    const uint8_t* s = bbuf + idx * FB + slot;
+    const uint8_t* s = bbuf + idx * FBB + fslot;
     uint32_t bits = 0u;
 #pragma unroll
-    for (int k = 0; k < L; ++k) bits |= (uint32_t)(in_range(slot + k * EW, FB) && s[k * EW] != 0) << k;
+    for (int k = 0; k < L; ++k) bits |= (uint32_t)(in_range(fslot + k * FW, FBB) && s[k * FW] != 0) << k;
     return bits;
   }
   template <int L>

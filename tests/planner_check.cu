@@ -40,15 +40,28 @@ bool bulk_shape_ok(const Plan& p) {
   using S = TbShape<EW, CT>;
   using ST = typename Est::Store;
   bool ok = tb_smem_bytes<Est, EW, CT>() <= kMaxSmemPerCta;
-  ok = ok && (S::FB * sizeof(ST)) % 128 == 0 && S::FB % 128 == 0 && tb_stage_bytes<Est, EW, CT>() % 128 == 0;
+  ok = ok && (S::FB * sizeof(ST)) % 128 == 0 && S::FBB % 128 == 0 && tb_stage_bytes<Est, EW, CT>() % 128 == 0;
   ok = ok && (CT - 1) * S::CS + (EW - 1) + (S::L - 1) * EW == S::FB - 1;
-  ok = ok && S::TILE <= 256 && (EW * (int)sizeof(ST)) % 16 == 0 && EW % 16 == 0;
+  // largest flag index: chunk CT - 1, our EW at offset FW - EW of the FW-wide copy, step L - 1
+  ok = ok && (CT - 1) * S::L * S::FW + (S::FW - EW) + (EW - 1) + (S::L - 1) * S::FW == S::FBB - 1;
+  ok = ok && S::TILE <= 256 && (EW * (int)sizeof(ST)) % 16 == 0 && S::FW % 16 == 0 && S::FW >= EW;
   ok = ok && p.tile == S::TILE && p.block == S::BLOCK;
   return ok;
 }
 
 template <class Est>
 bool bulk_ok(const Plan& p) {
+  if constexpr (sizeof(typename Est::Store) == 4) {
+    if (p.env_width == 8) {
+      switch (p.width) {
+        case 4: return bulk_shape_ok<Est, 8, 4>(p);
+        case 8: return bulk_shape_ok<Est, 8, 8>(p);
+        case 16: return bulk_shape_ok<Est, 8, 16>(p);
+        case 32: return bulk_shape_ok<Est, 8, 32>(p);
+        default: return false;
+      }
+    }
+  }
   if (p.env_width != 32) return false;
   switch (p.width) {
     case 1: return bulk_shape_ok<Est, 32, 1>(p);
@@ -139,7 +152,10 @@ int main() {
               }
               if (p.tm_bulk) {
                 const bool b16 = (flags & RLCA_BF16) != 0;
-                bool ok = bulk && tm && E % 16 == 0 && T % 8 == 0 && E >= 64L * sms;
+                bool ok = bulk && tm && E % 16 == 0 && T % 8 == 0 &&
+                          (p.env_width == 32 ? E >= 64L * sms
+                                             : (p.env_width == 8 && !b16 && E < 64L * sms && p.nseg == 1 &&
+                                                p.ntiles >= 4));
                 switch (kind) {
                   case Kind::Gae: ok = ok && (b16 ? bulk_ok<GaeEst<true, bf16>>(p) : bulk_ok<GaeEst<true>>(p)); break;
                   case Kind::ValueTargets:

@@ -41,6 +41,7 @@ cases = [
     ("retrace", 20, 700, False, True, False), ("retrace", 70, 300, True, True, False),
     ("retrace", 3, 40000, True, False, False), ("retrace", 33, 130, False, False, True),
     ("retrace", 1000, 1000, True, False, False), ("retrace", 13, 2048, True, False, True),
+    ("gae", 2432, 1032, True, False, False), ("vtrace", 4096, 1024, True, False, False),
     ("vtrace", 9744, 64, True, False, False), ("vt", 10240, 520, True, False, False),
 ]
 worst = 0.0

@@ -553,6 +553,24 @@ def test_time_major_tile_copies_leave_status_clean(cuda_lib, kind, E, T):
 
 
 @pytest.mark.parametrize("kind", ["gae", "vt", "vtrace", "td", "disc", "elig", "psum_i32", "affine_fwd"])
+@pytest.mark.parametrize("E,T", [(16, 8), (1024, 520), (2432, 2048), (4096, 1024), (4096, 2056), (9712, 1024),
+                                 (4096, 128)])
+def test_time_major_narrow_tile_copies(cuda_lib, kind, E, T):
+    """Float32 time-major calls below 64 environments per SM with E % 16 ==
+    0, aligned inputs, two or more float inputs, rows of four or more tiles
+    and E / 8 >= 2 per SM move tiles of 8 environments by tensor copies; the
+    flag rows are copied 16 environments wide and each CTA reads its half
+    (odd CTAs the upper one).  The other shapes here take the other drivers;
+    results match the oracle and the device status word stays 0."""
+    st = C.c_uint(0)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    parity.check_case(kind, E, T, seed=E + T + 1, time_major=True, p_term=0.02)
+    parity.check_case(kind, E, T, seed=E + T + 2, time_major=True, inputs_ready=True)
+    assert cuda_lib.rlca_device_status(C.byref(st), 1) == _lib.RLCA_OK
+    assert st.value == 0, f"device status {st.value:#x}"
+
+
+@pytest.mark.parametrize("kind", ["gae", "vt", "vtrace", "td", "disc", "elig", "psum_i32", "affine_fwd"])
 @pytest.mark.parametrize("E,T", [(8, 64), (1000, 520), (4096, 2048), (256, 4096)])
 def test_time_major_few_envs_repeated_calls(cuda_lib, kind, E, T):
     """Time-major calls with few environments and rows of several tiles (the
